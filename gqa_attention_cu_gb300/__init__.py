@@ -1,0 +1,149 @@
+"""Packed variable-length GQA attention for GB300 (sm_103a).
+
+A thin ctypes binding over ``libpva.so`` (declared in ``include/pva.h``):
+the functions below only marshal arguments -- every step of the computation
+runs in the library's CUDA kernels.  There is no CPU fallback: if the
+compiled library is missing, every call raises.
+
+PyTorch provides device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import workloads  # noqa: F401  (seeded synthetic inputs)
+
+__all__ = ["pva_forward", "pva_get_status", "pva_schedule", "pva_status_string",
+           "pva_last_error", "pva_release", "pva_version", "load_library", "build",
+           "PvaError", "DTYPE_CODES", "DEV_FLAGS"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpva.so")
+
+PVA_OK, PVA_ERR_INVALID_ARG, PVA_ERR_UNSUPPORTED, PVA_ERR_CUDA, PVA_ERR_OOM = 0, -1, -2, -3, -4
+DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
+DEV_FLAGS = {"cu_q_start": 0x1, "cu_kv_start": 0x2, "cu_q_order": 0x4, "cu_kv_order": 0x8,
+             "too_many": 0x10, "wait_timeout": 0x100}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PvaError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"pva error {code}: {message}")
+        self.code = code
+
+
+def build(force: bool = False) -> str:
+    """Compile libpva.so in-tree (nvcc, sm_103a)."""
+    from ._build import build as _b
+    return _b(force=force)
+
+
+def load_library(path: str | None = None):
+    """Load libpva.so and declare its C signatures.  Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise PvaError(PVA_ERR_CUDA, f"{p} not found: build it with "
+                           "`python -m gqa_attention_cu_gb300._build`")
+        lib = ctypes.CDLL(p)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.pva_forward.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, f, i, vp]
+        lib.pva_forward.restype = i
+        lib.pva_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+        lib.pva_get_status.restype = i
+        lib.pva_schedule.argtypes = [vp, vp, i, i, i, i, i, i, i,
+                                     ctypes.POINTER(ctypes.c_int32), ctypes.c_size_t, vp]
+        lib.pva_schedule.restype = i
+        lib.pva_status_string.argtypes = [i]
+        lib.pva_status_string.restype = ctypes.c_char_p
+        lib.pva_last_error.argtypes = []
+        lib.pva_last_error.restype = ctypes.c_char_p
+        lib.pva_release.argtypes = []
+        lib.pva_release.restype = None
+        lib.pva_version.argtypes = []
+        lib.pva_version.restype = i
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != PVA_OK:
+        lib = load_library()
+        raise PvaError(rc, f"{lib.pva_status_string(rc).decode()}: {lib.pva_last_error().decode()}")
+
+
+def _stream_ptr(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    codes = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+    if t.dtype not in codes:
+        raise PvaError(PVA_ERR_INVALID_ARG, f"dtype {t.dtype} not supported (f32, f16, bf16)")
+    return codes[t.dtype]
+
+
+def pva_forward(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B: int, num_heads: int,
+                kv_num_heads: int, head_size: int, v_head_size: int, scale: float = 0.0,
+                is_causal: int = 0, softcap: float = 0.0, dtype: int | None = None,
+                stream=None) -> None:
+    """Enqueue out = attention(q, k, v) on ``stream`` (torch stream, raw
+    cudaStream_t int, or None for the current stream).  Tensors are CUDA
+    tensors; their data pointers are passed as they are (contiguous layouts
+    as in include/pva.h)."""
+    lib = load_library()
+    code = _dtype_code(q) if dtype is None else int(dtype)
+    rc = lib.pva_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), cu_seqlens_q.data_ptr(),
+                         cu_seqlens_kv.data_ptr(), out.data_ptr(), int(B), int(num_heads),
+                         int(kv_num_heads), int(head_size), int(v_head_size), float(scale),
+                         int(is_causal), float(softcap), code, _stream_ptr(stream))
+    _check(rc)
+
+
+def pva_get_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) its latched device bits."""
+    lib = load_library()
+    flags = ctypes.c_uint32(0)
+    _check(lib.pva_get_status(_stream_ptr(stream), ctypes.byref(flags)))
+    return int(flags.value)
+
+
+def pva_schedule(cu_seqlens_q, cu_seqlens_kv, B: int, num_heads: int, kv_num_heads: int,
+                 head_size: int, v_head_size: int, is_causal: int, dtype: int, stream=None):
+    """Run only the on-device scheduler; returns its int32 words as a list."""
+    lib = load_library()
+    n = 8 + 4 * int(B) + 2
+    buf = (ctypes.c_int32 * n)()
+    _check(lib.pva_schedule(cu_seqlens_q.data_ptr(), cu_seqlens_kv.data_ptr(), int(B),
+                            int(num_heads), int(kv_num_heads), int(head_size), int(v_head_size),
+                            int(is_causal), int(dtype), buf, n, _stream_ptr(stream)))
+    return list(buf)
+
+
+def pva_status_string(code: int) -> str:
+    return load_library().pva_status_string(int(code)).decode()
+
+
+def pva_last_error() -> str:
+    return load_library().pva_last_error().decode()
+
+
+def pva_release() -> None:
+    load_library().pva_release()
+
+
+def pva_version() -> int:
+    return int(load_library().pva_version())

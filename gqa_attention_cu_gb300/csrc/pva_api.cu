@@ -1,0 +1,362 @@
+// Host side of libpva: argument checks, per-(device, stream) workspaces,
+// TMA tensor maps, and the launches of the scheduler and compute kernels.
+//
+// Argument rules follow the op's schema and the checks of its `execute`
+// (packed_varlen_attention.rs: dtypes f32/f16/bf16, num_heads and
+// kv_num_heads positive with kv_num_heads dividing num_heads, default scale
+// 1/sqrt(head_size) computed in f32).  The offsets themselves are checked on
+// the device (pva_scheduler.cu), so no call copies anything back to the host.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+
+#include "pva_internal.h"
+
+using namespace pva;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PVA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+  int num_sms = 0;
+  bool ready = false;
+};
+
+struct Workspace {
+  uint32_t* status = nullptr;  // sticky status word (never moves)
+  void* buf = nullptr;         // int region + partials
+  size_t bytes = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_dev;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_info(int dev, DeviceInfo* out) {
+  auto& d = g_dev[dev];
+  if (!d.ready) {
+    cudaError_t e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.ready = true;
+  }
+  *out = d;
+  return PVA_OK;
+}
+
+int get_encoder() {
+  if (g_encode) return PVA_OK;
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+    return fail(PVA_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return PVA_OK;
+}
+
+// Rank-3 map over a packed [tokens, heads, dim] tensor of 16-bit elements.
+// The token extent is set to INT32_MAX: the kernels never address a token
+// outside [0, cu[B]) (tiles are shifted back at the end of the buffer and
+// negative starts are zero-filled), so the extent is only a bound.
+int encode_map(CUtensorMap* map, const void* base, int dtype, int dim, int heads, int box_dim,
+               int box_heads, int box_tokens, bool swizzle128) {
+  const cuuint64_t gdim[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)INT32_MAX};
+  const cuuint64_t gstride[2] = {(cuuint64_t)dim * 2, (cuuint64_t)dim * heads * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)box_dim, (cuuint32_t)box_heads, (cuuint32_t)box_tokens};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = g_encode(map, dtype == PVA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void*>(base), gdim, gstride, box, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char msg[160];
+    snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled failed (%d) dim=%d heads=%d box=%dx%dx%d",
+             (int)r, dim, heads, box_dim, box_heads, box_tokens);
+    return fail(PVA_ERR_CUDA, msg);
+  }
+  return PVA_OK;
+}
+
+struct Plan {
+  bool tensor_core = false;  // bf16/f16 tcgen05 prefill
+  bool decode = false;       // split-KV decode kernel for L_q == 1
+  SchedConfig sched{};
+  size_t int_bytes = 0, partial_bytes = 0;
+  int cap_units = 0;
+};
+
+int check_and_plan(const void* q, const void* k, const void* v, const int32_t* cu_q,
+                   const int32_t* cu_kv, void* out, int B, int H, int Hkv, int d, int dv,
+                   float scale, float softcap, int dtype, Plan* plan) {
+  if (!q || !k || !v || !cu_q || !cu_kv || !out)
+    return fail(PVA_ERR_INVALID_ARG, "null pointer argument");
+  if (B < 1) return fail(PVA_ERR_INVALID_ARG, "B must be >= 1");
+  if (H <= 0 || Hkv <= 0 || H % Hkv != 0)
+    return fail(PVA_ERR_INVALID_ARG,
+                "num_heads must be a positive multiple of a positive kv_num_heads");
+  if (dtype != PVA_F32 && dtype != PVA_F16 && dtype != PVA_BF16)
+    return fail(PVA_ERR_INVALID_ARG, "dtype must be 0 (f32), 1 (f16) or 2 (bf16)");
+  if (!isfinite(scale) || !isfinite(softcap))
+    return fail(PVA_ERR_INVALID_ARG, "scale and softcap must be finite");
+  if (d <= 0 || dv <= 0) return fail(PVA_ERR_INVALID_ARG, "head sizes must be positive");
+  const int G = H / Hkv;
+  if (dtype == PVA_F32) {
+    if (d > 256 || dv > 256)
+      return fail(PVA_ERR_UNSUPPORTED, "f32 path supports head sizes up to 256");
+    plan->sched = SchedConfig{kF32TileTokens, H, kF32KeyTile, 0, 0};
+  } else {
+    if (d != dv || (d != 64 && d != 128 && d != 256))
+      return fail(PVA_ERR_UNSUPPORTED,
+                  "f16/bf16 path supports head_size == v_head_size in {64, 128, 256}");
+    if (G > kTcRows)
+      return fail(PVA_ERR_UNSUPPORTED, "f16/bf16 path supports num_heads/kv_num_heads <= 128");
+    const uintptr_t mis = (uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)out;
+    if (mis & 15) return fail(PVA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+    plan->tensor_core = true;
+    plan->decode = (G == 1 || G == 2 || G == 4 || G == 8);
+    plan->sched = SchedConfig{kTcRows / G, Hkv, tc_block_n(d), plan->decode ? 1 : 0, 0};
+  }
+  const WsLayout L{B, Hkv};
+  plan->int_bytes = L.int_words() * 4;
+  if (plan->decode) {
+    long long cap = (long long)B * Hkv * kDecodeMaxSplits;
+    if (cap > 16384) cap = 16384;
+    plan->cap_units = (int)cap;
+    plan->partial_bytes = (size_t)cap * (size_t)(G * dv + 2 * G) * sizeof(float);
+  }
+  return PVA_OK;
+}
+
+int get_workspace(int dev, cudaStream_t stream, size_t need, Workspace** out) {
+  Workspace& w = g_ws[{dev, stream}];
+  if (!w.status) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(stream, &cs);
+    if (cs != cudaStreamCaptureStatusNone)
+      return fail(PVA_ERR_INVALID_ARG,
+                  "first call on a stream must not be captured (workspace allocation)");
+    cudaError_t e = cudaMalloc(&w.status, 256);
+    if (e != cudaSuccess) return fail(PVA_ERR_OOM, "status word allocation failed");
+    e = cudaMemset(w.status, 0, 256);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+  }
+  if (w.bytes < need) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(stream, &cs);
+    if (cs != cudaStreamCaptureStatusNone)
+      return fail(PVA_ERR_INVALID_ARG,
+                  "workspace must grow but the stream is being captured; warm it up first");
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    if (w.buf) cudaFree(w.buf);
+    w.buf = nullptr;
+    w.bytes = 0;
+    size_t sz = need < (1u << 20) ? (1u << 20) : need;
+    e = cudaMalloc(&w.buf, sz);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(PVA_ERR_OOM, "workspace allocation failed");
+    }
+    w.bytes = sz;
+  }
+  *out = &w;
+  return PVA_OK;
+}
+
+int prepare(const void* q, const void* k, const void* v, const int32_t* cu_q,
+            const int32_t* cu_kv, void* out, int B, int H, int Hkv, int d, int dv, float scale,
+            int is_causal, float softcap, int dtype, cudaStream_t stream, Plan* plan,
+            AttnParams* p, int* num_sms) {
+  int rc = check_and_plan(q, k, v, cu_q, cu_kv, out, B, H, Hkv, d, dv, scale, softcap, dtype,
+                          plan);
+  if (rc != PVA_OK) return rc;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceInfo di;
+  rc = device_info(dev, &di);
+  if (rc != PVA_OK) return rc;
+  *num_sms = di.num_sms;
+  plan->sched.num_sms = di.num_sms;
+  Workspace* w = nullptr;
+  rc = get_workspace(dev, stream, plan->int_bytes + plan->partial_bytes, &w);
+  if (rc != PVA_OK) return rc;
+
+  AttnParams& P = *p;
+  P.q = q;
+  P.k = k;
+  P.v = v;
+  P.out = out;
+  P.cu_q = cu_q;
+  P.cu_kv = cu_kv;
+  P.B = B;
+  P.H = H;
+  P.Hkv = Hkv;
+  P.G = H / Hkv;
+  P.d = d;
+  P.dv = dv;
+  // scale 0 selects the default 1/sqrt(head_size), computed in f32 as the
+  // page does; softcap's sign does not matter (c * tanh(s / c) is even in c).
+  P.scale = scale != 0.0f ? scale : 1.0f / sqrtf((float)d);
+  P.softcap = fabsf(softcap);
+  P.is_causal = is_causal ? 1 : 0;
+  P.status = w->status;
+  P.ws = static_cast<int32_t*>(w->buf);
+  P.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(w->buf) + plan->int_bytes);
+  P.dec_cap_units = plan->cap_units;
+  return PVA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pva_forward(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                const int32_t* cu_seqlens_kv, void* out, int B, int num_heads, int kv_num_heads,
+                int head_size, int v_head_size, float scale, int is_causal, float softcap,
+                int dtype, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  std::lock_guard<std::mutex> lock(g_mu);
+  Plan plan;
+  AttnParams p{};
+  int num_sms = 0;
+  int rc = prepare(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B, num_heads, kv_num_heads,
+                   head_size, v_head_size, scale, is_causal, softcap, dtype, stream, &plan, &p,
+                   &num_sms);
+  if (rc != PVA_OK) return rc;
+
+  CUtensorMap tq, tk, tv, dk, dvm;
+  if (plan.tensor_core) {
+    if ((rc = get_encoder()) != PVA_OK) return rc;
+    const int G = p.G, m = kTcRows / G, bn = tc_block_n(head_size);
+    if ((rc = encode_map(&tq, q, dtype, head_size, num_heads, 64, G, m, true)) != PVA_OK ||
+        (rc = encode_map(&tk, k, dtype, head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK ||
+        (rc = encode_map(&tv, v, dtype, v_head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK)
+      return rc;
+    if (plan.decode) {
+      const int tkeys = decode_tile_keys(head_size);
+      if ((rc = encode_map(&dk, k, dtype, head_size, kv_num_heads, head_size, 1, tkeys,
+                           false)) != PVA_OK ||
+          (rc = encode_map(&dvm, v, dtype, v_head_size, kv_num_heads, v_head_size, 1, tkeys,
+                           false)) != PVA_OK)
+        return rc;
+    }
+  }
+
+  cudaError_t e = launch_scheduler(p, plan.sched, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "scheduler launch");
+  if (!plan.tensor_core) {
+    e = launch_prefill_f32(p, num_sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fp32 attention launch");
+    return PVA_OK;
+  }
+  e = launch_prefill_tc(p, dtype, tq, tk, tv, num_sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
+  if (plan.decode) {
+    e = launch_decode(p, dtype, dk, dvm, num_sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "split-KV decode launch");
+  }
+  return PVA_OK;
+}
+
+int pva_get_status(void* stream_, uint32_t* device_flags) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (!device_flags) return fail(PVA_ERR_INVALID_ARG, "device_flags is null");
+  *device_flags = 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  auto it = g_ws.find({dev, stream});
+  if (it == g_ws.end() || !it->second.status) return PVA_OK;
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t v = 0;
+  e = cudaMemcpy(&v, it->second.status, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy status");
+  e = cudaMemset(it->second.status, 0, sizeof v);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemset status");
+  *device_flags = v;
+  return PVA_OK;
+}
+
+int pva_schedule(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int B, int num_heads,
+                 int kv_num_heads, int head_size, int v_head_size, int is_causal, int dtype,
+                 int32_t* host_out, size_t capacity, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (!host_out) return fail(PVA_ERR_INVALID_ARG, "host_out is null");
+  if (B >= 1 && capacity < (size_t)8 + 4 * (size_t)B + 2)
+    return fail(PVA_ERR_INVALID_ARG, "host_out capacity too small");
+  std::lock_guard<std::mutex> lock(g_mu);
+  Plan plan;
+  AttnParams p{};
+  int num_sms = 0;
+  // q/k/v/out are not touched by the scheduler; aligned placeholders satisfy
+  // the pointer checks.
+  const void* dummy = reinterpret_cast<const void*>(uintptr_t(256));
+  int rc = prepare(dummy, dummy, dummy, cu_seqlens_q, cu_seqlens_kv, const_cast<void*>(dummy), B,
+                   num_heads, kv_num_heads, head_size, v_head_size, 1.0f, is_causal, 0.0f, dtype,
+                   stream, &plan, &p, &num_sms);
+  if (rc != PVA_OK) return rc;
+  cudaError_t e = launch_scheduler(p, plan.sched, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "scheduler launch");
+  const size_t words = 8 + 4 * (size_t)B + 2;
+  e = cudaMemcpyAsync(host_out, p.ws, words * 4, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  return PVA_OK;
+}
+
+const char* pva_status_string(int code) {
+  switch (code) {
+    case PVA_OK: return "ok";
+    case PVA_ERR_INVALID_ARG: return "invalid argument";
+    case PVA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PVA_ERR_CUDA: return "CUDA error";
+    case PVA_ERR_OOM: return "out of device memory";
+    default: return "unknown status";
+  }
+}
+
+const char* pva_last_error(void) { return g_last_error.c_str(); }
+
+void pva_release(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return;
+  cudaDeviceSynchronize();
+  for (auto it = g_ws.begin(); it != g_ws.end();) {
+    if (it->first.first == dev) {
+      if (it->second.buf) cudaFree(it->second.buf);
+      if (it->second.status) cudaFree(it->second.status);
+      it = g_ws.erase(it);
+    } else {
+      ++it;
+    }
+  }
+}
+
+int pva_version(void) { return (0 << 16) | (1 << 8) | 0; }
+
+}  // extern "C"

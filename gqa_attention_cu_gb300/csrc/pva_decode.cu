@@ -1,0 +1,404 @@
+// Split-KV decode for sequences with a single query token (L_q == 1), bf16 or
+// f16, head size d = dv in {64, 128, 256}, H/Hkv = G in {1, 2, 4, 8}.
+//
+// With one query row the tail-aligned causal frontier (packed_varlen_
+// attention.rs, "Causal alignment") is L_kv - 1, so every key is visible and
+// the work is a pass over the sequence's K and V rows: it is bound by HBM
+// bandwidth, and each K/V row is read once for all G query heads that share
+// it.
+//
+// Work unit = (sequence, kv head g, split s): the keys of a sequence are cut
+// into S_b splits (chosen on the device by the scheduler).  Per CTA
+// (persistent, one per SM):
+//   warp 0      TMA producer: K and V tiles of TK keys (16 KB each, rows of
+//               d contiguous elements) into a 4-stage ring.
+//   warps 1..8  compute.  A round covers R = 32/G keys x G heads = 32
+//               (key, head) pairs: lane l owns d/32 consecutive dims of every
+//               key, forms the 32 partial dot products, and a reduce-scatter
+//               butterfly (warp shuffles) leaves the full score of pair l in
+//               lane l.  Online softmax per head, probabilities shared
+//               through shared memory, O accumulated per lane over its dims.
+//   end of unit the 8 warps' (max, sum, O) are merged in a fixed order;
+//               an unsplit unit writes the output row; a split unit writes
+//               its fp32 partial and the last split to finish (device-wide
+//               counter) combines all splits in split order (log-sum-exp
+//               combine) and writes the output, so results do not depend on
+//               which CTA finishes last.
+#include "pva_device.cuh"
+
+namespace pva {
+namespace {
+
+constexpr int kComputeWarps = 8;
+constexpr int kThreads = 32 * (1 + kComputeWarps);
+constexpr int kStages = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D, int G>
+struct DecCfg {
+  static constexpr int TK = decode_tile_keys(D);   // keys per tile
+  static constexpr int DPL = D / 32;               // dims per lane
+  static constexpr int R = 32 / G;                 // keys per round
+  static constexpr int RPT = TK / R;               // rounds per tile
+  static constexpr int TILE_BYTES = TK * D * 2;
+  static constexpr int OFF_KV = 0;
+  static constexpr int OFF_O = kStages * 2 * TILE_BYTES;             // [8][G][D] fp32
+  static constexpr int OFF_ML = OFF_O + kComputeWarps * G * D * 4;   // [8][G] m, [8][G] l
+  static constexpr int OFF_P = OFF_ML + 2 * kComputeWarps * G * 4;   // [8][32] p
+  static constexpr int OFF_A = OFF_P + kComputeWarps * 32 * 4;       // [8][G] alpha
+  static constexpr int OFF_BAR = OFF_A + kComputeWarps * G * 4;
+  static constexpr int SMEM = OFF_BAR + 2 * kStages * 8 + 128;
+  static_assert(RPT >= 1, "tile shorter than a round");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct Unit {
+  int b, g, s, S;      // sequence, kv head, split index, split count
+  int ks, ke;          // key range [ks, ke) local to the sequence
+  int kv_start, q_tok;
+};
+
+__device__ __forceinline__ Unit decode_unit(const AttnParams& p, const SchedHeader& h, int u) {
+  const WsLayout L{p.B, p.Hkv};
+  const int32_t* order = p.ws + L.dec_order();
+  const int32_t* prefix = p.ws + L.dec_prefix();
+  int lo = 0, hi = h.n_dec - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  Unit r;
+  r.b = order[lo];
+  r.S = (prefix[lo + 1] - prefix[lo]) / p.Hkv;
+  const int local = u - prefix[lo];
+  r.g = local / r.S;
+  r.s = local - r.g * r.S;
+  r.kv_start = p.cu_kv[r.b];
+  r.q_tok = p.cu_q[r.b];
+  const int lkv = p.cu_kv[r.b + 1] - r.kv_start;
+  const int per = (lkv + r.S - 1) / r.S;
+  r.ks = min(lkv, r.s * per);
+  r.ke = min(lkv, r.ks + per);
+  return r;
+}
+
+__device__ __forceinline__ void compute_bar_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kComputeWarps * 32) : "memory");
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void load_dims(const uint8_t* row, int lane, float (&f)[N]) {
+  // N consecutive 16-bit values at element offset lane * N.
+  const uint8_t* src = row + lane * N * 2;
+  if constexpr (N == 2) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
+    const float2 a = unpack2<T>(w);
+    f[0] = a.x; f[1] = a.y;
+  } else if constexpr (N == 4) {
+    const uint2 w = *reinterpret_cast<const uint2*>(src);
+    const float2 a = unpack2<T>(w.x), b = unpack2<T>(w.y);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  } else {
+    const uint4 w = *reinterpret_cast<const uint4*>(src);
+    const float2 a = unpack2<T>(w.x), b = unpack2<T>(w.y), c = unpack2<T>(w.z),
+                 d = unpack2<T>(w.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+  }
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    pva_decode_kernel(AttnParams p, const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v) {
+  using C = DecCfg<D, G>;
+  constexpr int TK = C::TK, DPL = C::DPL, R = C::R;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~uintptr_t(127));
+  float* sO = reinterpret_cast<float*>(smem + C::OFF_O);
+  float* sM = reinterpret_cast<float*>(smem + C::OFF_ML);
+  float* sL = sM + kComputeWarps * G;
+  float* sP = reinterpret_cast<float*>(smem + C::OFF_P);
+  float* sA = reinterpret_cast<float*>(smem + C::OFF_A);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + kStages;
+  __shared__ int s_abort, s_last;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const SchedHeader h = *reinterpret_cast<const SchedHeader*>(p.ws + kWsHeader);
+  uint32_t* status = p.status;
+  volatile int* abort = &s_abort;
+  const int total_kv = p.cu_kv[p.B];
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kComputeWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensor_map(&tmap_k);
+      prefetch_tensor_map(&tmap_v);
+      uint32_t cnt = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < h.n_units; u += gridDim.x) {
+        const Unit un = decode_unit(p, h, u);
+        const int nt = (un.ke - un.ks + TK - 1) / TK;
+        for (int j = 0; j < nt; ++j, ++cnt) {
+          const int st = cnt % kStages;
+          if (!(ok = mbar_wait(&empty[st], ((cnt / kStages) & 1) ^ 1, abort, status))) break;
+          const int k0 = min(un.kv_start + un.ks + j * TK, total_kv - TK);
+          uint8_t* dk = smem + C::OFF_KV + st * 2 * C::TILE_BYTES;
+          mbar_arrive_expect_tx(&full[st], 2 * C::TILE_BYTES);
+          tma_load_3d(dk, &tmap_k, &full[st], 0, un.g, k0);
+          tma_load_3d(dk + C::TILE_BYTES, &tmap_v, &full[st], 0, un.g, k0);
+        }
+      }
+      for (int s = 0; s < kStages; ++s) {
+        const uint32_t fills = cnt > (uint32_t)s ? (cnt - 1 - s) / kStages + 1 : 0;
+        if (fills) mbar_wait(&full[s], (fills - 1) & 1, abort, status);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ compute
+    const int cw = warp - 1;  // compute warp 0..7
+    const float NEG_INF = __int_as_float(0xff800000);
+    const bool capped = p.softcap != 0.0f;
+    const float qmul = capped ? p.scale / p.softcap : p.scale * kLog2e;
+    const float cap_mul = p.softcap * kLog2e;
+    const int my_r = lane / G, my_h = lane % G;  // pair owned after the reduce-scatter
+    T* out = static_cast<T*>(p.out);
+    uint32_t cnt = 0;
+    bool ok = true;
+
+    for (int u = blockIdx.x; ok && u < h.n_units; u += gridDim.x) {
+      const Unit un = decode_unit(p, h, u);
+      const int nt = (un.ke - un.ks + TK - 1) / TK;
+
+      float q[G][DPL];
+      {
+        const T* Q = static_cast<const T*>(p.q);
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          const uint8_t* row = reinterpret_cast<const uint8_t*>(
+              Q + ((size_t)un.q_tok * p.H + (size_t)un.g * G + hh) * D);
+          load_dims<T, DPL>(row, lane, q[hh]);
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) q[hh][e] *= qmul;
+        }
+      }
+      float acc[G][DPL];
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[hh][e] = 0.0f;
+      float m_run = NEG_INF, l_part = 0.0f;
+
+      for (int j = 0; j < nt; ++j, ++cnt) {
+        const int st = cnt % kStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (cnt / kStages) & 1, abort, status));
+        if (!ok) break;
+        const uint8_t* sK = smem + C::OFF_KV + st * 2 * C::TILE_BYTES;
+        const uint8_t* sV = sK + C::TILE_BYTES;
+        const int k0 = min(un.kv_start + un.ks + j * TK, total_kv - TK);
+        const int base = k0 - un.kv_start;            // local key of tile row 0
+        const int lo = un.ks + j * TK - base;          // visible tile rows [lo, hi)
+        const int hi = min(un.ks + (j + 1) * TK, un.ke) - base;
+        for (int rd = cw; rd < C::RPT; rd += kComputeWarps) {
+          const int r0 = rd * R;  // first tile row of this round
+          float v[32];
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            float kf[DPL];
+            load_dims<T, DPL>(sK + (size_t)(r0 + r) * D * 2, lane, kf);
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+              float a = 0.0f;
+#pragma unroll
+              for (int e = 0; e < DPL; ++e) a = fmaf(q[hh][e], kf[e], a);
+              v[r * G + hh] = a;
+            }
+          }
+          // reduce-scatter: after the 5 steps lane l holds the full dot of pair l
+#pragma unroll
+          for (int step = 16; step >= 1; step >>= 1) {
+            const bool upper = (lane & step) != 0;
+#pragma unroll
+            for (int i = 0; i < step; ++i) {
+              const float send = upper ? v[i] : v[i + step];
+              const float keep = upper ? v[i + step] : v[i];
+              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, step);
+            }
+          }
+          const int row = r0 + my_r;
+          float x = capped ? cap_mul * tanh_via_exp2(v[0]) : v[0];
+          x = (row >= lo && row < hi) ? x : NEG_INF;
+          float mr = x;
+#pragma unroll
+          for (int o = G; o < 32; o <<= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+          const float m_new = fmaxf(m_run, mr);
+          float alpha = 1.0f, pr = 0.0f;
+          if (m_new != NEG_INF) {
+            alpha = ex2_approx(m_run - m_new);
+            pr = ex2_approx(x - m_new);
+          }
+          m_run = m_new;
+          l_part = l_part * alpha + pr;
+          sP[cw * 32 + lane] = pr;
+          if (lane < G) sA[cw * G + lane] = alpha;
+          __syncwarp();
+#pragma unroll
+          for (int hh = 0; hh < G; ++hh) {
+            const float a = sA[cw * G + hh];
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[hh][e] *= a;
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            float vf[DPL];
+            load_dims<T, DPL>(sV + (size_t)(r0 + r) * D * 2, lane, vf);
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+              const float pw = sP[cw * 32 + r * G + hh];
+#pragma unroll
+              for (int e = 0; e < DPL; ++e) acc[hh][e] = fmaf(pw, vf[e], acc[hh][e]);
+            }
+          }
+          __syncwarp();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+
+      // per-head sum over this warp's lanes, then merge the 8 warps
+#pragma unroll
+      for (int o = G; o < 32; o <<= 1) l_part += __shfl_xor_sync(0xffffffffu, l_part, o);
+      if (lane < G) {
+        sM[cw * G + lane] = m_run;
+        sL[cw * G + lane] = l_part;
+      }
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) sO[(cw * G + hh) * D + lane * DPL + e] = acc[hh][e];
+      // Every compute warp reaches this barrier, whether it finished its tiles
+      // or gave up on a wait; the give-up decision is then read by all of
+      // them at once, so no warp is ever left alone at a named barrier.
+      compute_bar_sync();
+      if (*abort) break;
+
+      const int t = threadIdx.x - 32;  // 0..255
+      const bool split = un.S > 1;
+      float* part = p.partials + (size_t)u * (G * D + 2 * G);
+      for (int e = t; e < G * D; e += kComputeWarps * 32) {
+        const int hh = e / D;
+        float M = NEG_INF;
+#pragma unroll
+        for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, sM[w * G + hh]);
+        float Lsum = 0.0f, O = 0.0f;
+        if (M != NEG_INF) {
+#pragma unroll
+          for (int w = 0; w < kComputeWarps; ++w) {
+            const float sc = ex2_approx(sM[w * G + hh] - M);
+            Lsum += sL[w * G + hh] * sc;
+            O += sO[w * G * D + e] * sc;
+          }
+        }
+        if (!split) {
+          const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
+          out[((size_t)un.q_tok * p.H + (size_t)un.g * G) * D + e] = static_cast<T>(O * inv);
+        } else {
+          part[e] = O;
+          if (e - hh * D == 0) {
+            part[G * D + hh] = M;
+            part[G * D + G + hh] = Lsum;
+          }
+        }
+      }
+      if (split) {
+        __threadfence();
+        compute_bar_sync();
+        if (t == 0) {
+          const WsLayout L{p.B, p.Hkv};
+          int* done = p.ws + L.dec_done() + (size_t)un.b * p.Hkv + un.g;
+          s_last = atomicAdd(done, 1) == un.S - 1;
+        }
+        compute_bar_sync();
+        if (s_last) {
+          __threadfence();
+          const float* first = p.partials + (size_t)(u - un.s) * (G * D + 2 * G);
+          const size_t stride = G * D + 2 * G;
+          for (int e = t; e < G * D; e += kComputeWarps * 32) {
+            const int hh = e / D;
+            float M = NEG_INF;
+            for (int s = 0; s < un.S; ++s) M = fmaxf(M, __ldcg(first + s * stride + G * D + hh));
+            float Lsum = 0.0f, O = 0.0f;
+            if (M != NEG_INF) {
+              for (int s = 0; s < un.S; ++s) {
+                const float* ps = first + s * stride;
+                const float sc = ex2_approx(__ldcg(ps + G * D + hh) - M);
+                Lsum += __ldcg(ps + G * D + G + hh) * sc;
+                O += __ldcg(ps + e) * sc;
+              }
+            }
+            const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
+            out[((size_t)un.q_tok * p.H + (size_t)un.g * G) * D + e] = static_cast<T>(O * inv);
+          }
+        }
+      }
+      compute_bar_sync();  // shared merge buffers are reused by the next unit
+    }
+  }
+  __syncthreads();
+}
+
+template <typename T, int D, int G>
+cudaError_t launch_dec(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                       int num_sms, cudaStream_t s) {
+  constexpr int smem = DecCfg<D, G>::SMEM;
+  auto kern = pva_decode_kernel<T, D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<num_sms, kThreads, smem, s>>>(p, tk, tv);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_dec_g(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                         int num_sms, cudaStream_t s) {
+  switch (p.G) {
+    case 1: return launch_dec<T, D, 1>(p, tk, tv, num_sms, s);
+    case 2: return launch_dec<T, D, 2>(p, tk, tv, num_sms, s);
+    case 4: return launch_dec<T, D, 4>(p, tk, tv, num_sms, s);
+    case 8: return launch_dec<T, D, 8>(p, tk, tv, num_sms, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename T>
+cudaError_t launch_dec_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                         int num_sms, cudaStream_t s) {
+  switch (p.d) {
+    case 64: return launch_dec_g<T, 64>(p, tk, tv, num_sms, s);
+    case 128: return launch_dec_g<T, 128>(p, tk, tv, num_sms, s);
+    case 256: return launch_dec_g<T, 256>(p, tk, tv, num_sms, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const AttnParams& p, int dtype, const CUtensorMap& tk,
+                          const CUtensorMap& tv, int num_sms, cudaStream_t s) {
+  return dtype == PVA_BF16 ? launch_dec_t<__nv_bfloat16>(p, tk, tv, num_sms, s)
+                           : launch_dec_t<__half>(p, tk, tv, num_sms, s);
+}
+
+}  // namespace pva

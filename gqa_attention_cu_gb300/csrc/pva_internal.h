@@ -1,0 +1,100 @@
+// Internal definitions shared by the host launcher and the kernels of libpva:
+// the workspace layout written by the on-device scheduler, the parameter
+// block every kernel receives, tile constants and the launch functions.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "pva.h"
+
+#define PVA_WAIT_LIMIT_NS 2000000000ull  // 2 s: no legitimate pipeline wait comes close
+
+namespace pva {
+
+// ---- tile shapes ------------------------------------------------------------
+constexpr int kTcRows = 128;        // MMA rows per query tile (G heads x tokens)
+constexpr int kF32TileTokens = 16;  // query tokens per fp32 work item
+constexpr int kF32KeyTile = 32;     // keys per fp32 key/value tile
+constexpr int kDecodeMaxSplits = 16;
+constexpr int kDecodeMaxGroup = 8;  // largest H/Hkv served by the split-KV decode kernel
+constexpr int kSortMax = 2048;      // sequences sorted on device; more keep input order
+
+// Keys per tensor-core key/value tile for head size D.
+__host__ __device__ constexpr int tc_block_n(int D) { return D >= 256 ? 64 : 128; }
+// Keys per decode key/value tile for head size D (16 KB of K per tile).
+__host__ __device__ constexpr int decode_tile_keys(int D) { return 8192 / D; }
+
+// ---- workspace layout (int32 words) ----------------------------------------
+// [0..8)         SchedHeader of the latest call
+// [8..)          prefill order [B], prefill prefix [B+1], decode order [B],
+//                decode prefix [B+1], decode completion counters [B*Hkv]
+// then (256-byte aligned) fp32 split partials [cap_units][G*dv + 2G].
+// The sticky status word lives in its own allocation (it never moves when
+// the workspace grows).
+struct SchedHeader {
+  uint32_t status;     // PVA_DEV_* bits of this call
+  int32_t n_pref;      // sequences with prefill work, in pref_order
+  int32_t n_items;     // prefill work items
+  int32_t n_dec;       // sequences routed to split-KV decode, in dec_order
+  int32_t n_units;     // decode work units (sequence, kv head, split)
+  int32_t tile_tokens; // query tokens per prefill item
+  int32_t units_per_tile;  // items per query tile (kv heads or heads)
+  int32_t dec_chunk;   // keys per decode split
+};
+
+constexpr int kWsHeader = 0;
+constexpr int kWsArrays = 8;
+
+struct WsLayout {
+  int B, Hkv;
+  __host__ __device__ int pref_order() const { return kWsArrays; }
+  __host__ __device__ int pref_prefix() const { return kWsArrays + B; }
+  __host__ __device__ int dec_order() const { return kWsArrays + 2 * B + 1; }
+  __host__ __device__ int dec_prefix() const { return kWsArrays + 3 * B + 1; }
+  __host__ __device__ int dec_done() const { return kWsArrays + 4 * B + 2; }
+  __host__ __device__ size_t int_words() const {
+    size_t w = (size_t)kWsArrays + 4 * (size_t)B + 2 + (size_t)B * Hkv;
+    return (w + 63) / 64 * 64;
+  }
+};
+
+// ---- per-call parameter block ------------------------------------------------
+struct AttnParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  const int32_t* cu_q;
+  const int32_t* cu_kv;
+  int B, H, Hkv, G, d, dv;
+  float scale;    // resolved (default already applied)
+  float softcap;  // 0 = off
+  int is_causal;
+  uint32_t* status;   // sticky PVA_DEV_* bits (OR-ed, cleared by pva_get_status)
+  int32_t* ws;        // workspace int region
+  float* partials;    // decode split partials
+  int dec_cap_units;  // partial slots available
+};
+
+struct SchedConfig {
+  int tile_tokens;     // query tokens per prefill item
+  int units_per_tile;  // items per query tile
+  int block_n;         // keys per prefill key tile (cost model only)
+  int decode_enabled;  // route L_q == 1 sequences to the decode kernel
+  int num_sms;
+};
+
+// ---- launchers (defined next to their kernels) -------------------------------
+cudaError_t launch_scheduler(const AttnParams& p, const SchedConfig& c, cudaStream_t s);
+cudaError_t launch_prefill_f32(const AttnParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_prefill_tc(const AttnParams& p, int dtype, const CUtensorMap& tq,
+                              const CUtensorMap& tk, const CUtensorMap& tv, int num_sms,
+                              cudaStream_t s);
+cudaError_t launch_decode(const AttnParams& p, int dtype, const CUtensorMap& tk,
+                          const CUtensorMap& tv, int num_sms, cudaStream_t s);
+
+}  // namespace pva

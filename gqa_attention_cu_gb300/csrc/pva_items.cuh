@@ -1,0 +1,59 @@
+// Decoding of a work-item index into (sequence, query tile, unit) using the
+// scheduler's ordered list and prefix sums.  Every role of every kernel
+// decodes the same index the same way, so no item descriptor is stored.
+#pragma once
+
+#include "pva_internal.h"
+
+namespace pva {
+
+struct PrefillItem {
+  int b;         // sequence
+  int t;         // query tile within the sequence (tiles run last to first)
+  int unit;      // kv head (tensor-core kernel) or query head (fp32 kernel)
+  int q_start;   // cu_seqlens_q[b]
+  int kv_start;  // cu_seqlens_kv[b]
+  int lq, lkv;   // sequence lengths
+};
+
+// Largest p in [0, n) with prefix[p] <= it (prefix strictly increasing).
+__device__ __forceinline__ int find_segment(const int32_t* prefix, int n, int it) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= it) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ PrefillItem decode_prefill_item(const AttnParams& p,
+                                                           const SchedHeader& h, int it) {
+  const WsLayout L{p.B, p.Hkv};
+  const int32_t* order = p.ws + L.pref_order();
+  const int32_t* prefix = p.ws + L.pref_prefix();
+  const int pos = find_segment(prefix, h.n_pref, it);
+  const int local = it - prefix[pos];
+  PrefillItem r;
+  r.b = order[pos];
+  r.q_start = p.cu_q[r.b];
+  r.kv_start = p.cu_kv[r.b];
+  r.lq = p.cu_q[r.b + 1] - r.q_start;
+  r.lkv = p.cu_kv[r.b + 1] - r.kv_start;
+  const int n_tiles = (r.lq + h.tile_tokens - 1) / h.tile_tokens;
+  const int rank = local / h.units_per_tile;
+  r.unit = local - rank * h.units_per_tile;
+  r.t = n_tiles - 1 - rank;  // most expensive (latest) query tile first
+  return r;
+}
+
+// Number of key tiles of `block_n` keys an item must visit: keys beyond the
+// causal frontier of its last query row are never loaded.
+__device__ __forceinline__ int item_key_extent(const PrefillItem& it, int tile_tokens,
+                                               int is_causal) {
+  const int last_row = min((it.t + 1) * tile_tokens, it.lq) - 1;
+  int hi = it.lkv;
+  if (is_causal) hi = min(it.lkv, last_row + (it.lkv - it.lq) + 1);
+  return hi > 0 ? hi : 0;
+}
+
+}  // namespace pva

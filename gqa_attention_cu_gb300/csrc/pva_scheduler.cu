@@ -1,0 +1,276 @@
+// On-device tile scheduler.
+//
+// Turns cu_seqlens_q / cu_seqlens_kv (packed_varlen_attention.rs, "Packed
+// layout & cumulative offsets") into the work description the compute
+// kernels read, without copying anything back to the host:
+//
+//   * validation of the offsets (start at 0, non-decreasing -- the checks the
+//     page's `execute` performs on the host), latched as status bits; on any
+//     error the work lists are left empty so nothing is written;
+//   * a prefill list: sequences with L_q > 0 (L_q >= 2 when decode routing is
+//     on), longest key range first (ties by sequence index), with an inclusive
+//     prefix of their work-item counts ceil(L_q / tile_tokens) * units;
+//   * a decode list: sequences with L_q == 1 (when routing is on), longest
+//     first, each split into S_b key chunks, with a prefix of their
+//     (kv head, split) unit counts;
+//   * zeroed split-completion counters for the decode combine.
+//
+// One CTA of 1024 threads.  B <= 2048 sequences are sorted in shared memory
+// (bitonic); larger batches keep their input order.
+#include <limits.h>
+
+#include "pva_device.cuh"
+
+namespace pva {
+
+namespace {
+
+constexpr int kThreads = 1024;
+
+// Exclusive scan of one int64 per thread across the CTA; returns the
+// exclusive prefix and writes the CTA total to *total.
+__device__ long long block_exclusive_scan(long long v, long long* scratch, long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = scratch[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    scratch[lane] = w;  // inclusive per-warp totals
+  }
+  __syncthreads();
+  const long long warp_base = warp ? scratch[warp - 1] : 0;
+  const long long tot = scratch[31];
+  __syncthreads();
+  *total = tot;
+  return warp_base + x - v;
+}
+
+__device__ long long block_sum(long long v, long long* scratch) {
+  long long t;
+  block_exclusive_scan(v, scratch, &t);
+  return t;
+}
+
+struct SeqLens {
+  int lq, lkv;
+};
+
+__device__ __forceinline__ SeqLens seq_lens(const AttnParams& p, int b) {
+  SeqLens s;
+  s.lq = p.cu_q[b + 1] - p.cu_q[b];
+  s.lkv = p.cu_kv[b + 1] - p.cu_kv[b];
+  return s;
+}
+
+__device__ __forceinline__ int decode_splits(int lkv, int chunk) {
+  if (lkv <= chunk) return 1;
+  int s = (lkv + chunk - 1) / chunk;
+  return s < kDecodeMaxSplits ? s : kDecodeMaxSplits;
+}
+
+// Builds one ordered list (class 0 = prefill, 1 = decode) and its prefix.
+// Returns false when the work count overflows int32.
+__device__ bool build_list(const AttnParams& p, const SchedConfig& c, int cls, int chunk,
+                           int32_t* order, int32_t* prefix, int* n_out, int* total_out,
+                           unsigned long long* keys, long long* scratch) {
+  const int B = p.B;
+  auto member = [&](int b) -> bool {
+    SeqLens s = seq_lens(p, b);
+    if (s.lq <= 0) return false;
+    const bool is_dec = c.decode_enabled && s.lq == 1;
+    return cls == 1 ? is_dec : !is_dec;
+  };
+  auto work = [&](int b) -> long long {
+    SeqLens s = seq_lens(p, b);
+    if (cls == 0)
+      return (long long)((s.lq + c.tile_tokens - 1) / c.tile_tokens) * c.units_per_tile;
+    return (long long)decode_splits(s.lkv, chunk) * p.Hkv;
+  };
+
+  int n = 0;
+  if (B <= kSortMax) {
+    int N = 1;
+    while (N < B) N <<= 1;
+    for (int i = threadIdx.x; i < N; i += kThreads) {
+      unsigned long long key = ~0ull;
+      if (i < B && member(i)) {
+        SeqLens s = seq_lens(p, i);
+        key = ((unsigned long long)(unsigned)(INT_MAX - s.lkv) << 32) | (unsigned)i;
+      }
+      keys[i] = key;
+    }
+    __syncthreads();
+    for (int k = 2; k <= N; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = threadIdx.x; i < N; i += kThreads) {
+          const int ixj = i ^ j;
+          if (ixj > i) {
+            const unsigned long long a = keys[i], bb = keys[ixj];
+            const bool up = (i & k) == 0;
+            if ((a > bb) == up) {
+              keys[i] = bb;
+              keys[ixj] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    long long cnt = 0;
+    for (int i = threadIdx.x; i < B; i += kThreads) {
+      const bool valid = keys[i] != ~0ull;
+      order[i] = valid ? (int32_t)(keys[i] & 0xffffffffu) : -1;
+      cnt += valid;
+    }
+    n = (int)block_sum(cnt, scratch);
+  } else {
+    // Input order: compact the members with a scan over contiguous chunks.
+    const int per = (B + kThreads - 1) / kThreads;
+    const int lo = min(B, (int)threadIdx.x * per), hi = min(B, lo + per);
+    long long local = 0;
+    for (int b = lo; b < hi; ++b) local += member(b);
+    long long total;
+    long long pos = block_exclusive_scan(local, scratch, &total);
+    for (int b = lo; b < hi; ++b)
+      if (member(b)) order[pos++] = b;
+    __syncthreads();
+    n = (int)total;
+    for (int i = n + threadIdx.x; i < B; i += kThreads) order[i] = -1;
+  }
+  __syncthreads();
+
+  // Prefix of work counts in list order: contiguous chunk per thread.
+  const int per = (n + kThreads - 1) / kThreads;
+  const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
+  long long local = 0;
+  for (int i = lo; i < hi; ++i) local += work(order[i]);
+  long long total;
+  long long run = block_exclusive_scan(local, scratch, &total);
+  const bool fits = total <= (long long)INT_MAX;
+  if (fits) {
+    for (int i = lo; i < hi; ++i) {
+      prefix[i] = (int32_t)run;
+      run += work(order[i]);
+    }
+    for (int i = n + threadIdx.x; i <= B; i += kThreads) prefix[i] = (int32_t)total;
+  }
+  *n_out = n;
+  *total_out = fits ? (int)total : 0;
+  return fits;
+}
+
+__global__ void __launch_bounds__(kThreads) pva_schedule_kernel(AttnParams p, SchedConfig c) {
+  __shared__ unsigned long long keys[kSortMax];
+  __shared__ long long scratch[32];
+  __shared__ uint32_t s_status;
+  __shared__ int s_chunk;
+
+  const int B = p.B;
+  const WsLayout L{B, p.Hkv};
+  int32_t* ws = p.ws;
+  SchedHeader* hdr = reinterpret_cast<SchedHeader*>(ws + kWsHeader);
+
+  if (threadIdx.x == 0) {
+    uint32_t st = 0;
+    if (p.cu_q[0] != 0) st |= PVA_DEV_CU_Q_START;
+    if (p.cu_kv[0] != 0) st |= PVA_DEV_CU_KV_START;
+    s_status = st;
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < B; b += kThreads) {
+    if (p.cu_q[b + 1] < p.cu_q[b]) atomicOr(&s_status, PVA_DEV_CU_Q_ORDER);
+    if (p.cu_kv[b + 1] < p.cu_kv[b]) atomicOr(&s_status, PVA_DEV_CU_KV_ORDER);
+  }
+  // Completion counters of the decode combine start at zero every call.
+  int32_t* done = ws + L.dec_done();
+  for (long long i = threadIdx.x; i < (long long)B * p.Hkv; i += kThreads) done[i] = 0;
+  __syncthreads();
+
+  int n_pref = 0, n_items = 0, n_dec = 0, n_units = 0;
+  if (s_status == 0) {
+    // Decode chunk: aim for about 8 units per SM, never more partial slots
+    // than the workspace holds (all sequences unsplit if it must).
+    if (c.decode_enabled) {
+      long long keyrows = 0, cnt = 0;
+      for (int b = threadIdx.x; b < B; b += kThreads) {
+        SeqLens s = seq_lens(p, b);
+        if (s.lq == 1) {
+          keyrows += s.lkv;
+          cnt += 1;
+        }
+      }
+      keyrows = block_sum(keyrows, scratch) * p.Hkv;
+      cnt = block_sum(cnt, scratch);
+      long long target = (long long)c.num_sms * 8;
+      long long chunk = (keyrows + target - 1) / target;
+      chunk = ((chunk + 63) / 64) * 64;
+      if (chunk < 256) chunk = 256;
+      // grow the chunk until the split units fit the partial slots
+      for (int it = 0; it < 40; ++it) {
+        long long units = 0;
+        int any_split = 0;
+        for (int b = threadIdx.x; b < B; b += kThreads) {
+          SeqLens s = seq_lens(p, b);
+          if (s.lq == 1) {
+            int sp = decode_splits(s.lkv, chunk > INT_MAX ? INT_MAX : (int)chunk);
+            units += (long long)sp * p.Hkv;
+            any_split |= sp > 1;
+          }
+        }
+        units = block_sum(units, scratch);
+        const long long splits = block_sum(any_split, scratch);
+        if (splits == 0 || units <= p.dec_cap_units) break;
+        chunk *= 2;
+      }
+      if (threadIdx.x == 0) s_chunk = chunk > INT_MAX ? INT_MAX : (int)chunk;
+      (void)cnt;
+    } else if (threadIdx.x == 0) {
+      s_chunk = INT_MAX;
+    }
+    __syncthreads();
+    const int chunk = s_chunk;
+    bool ok = build_list(p, c, 0, chunk, ws + L.pref_order(), ws + L.pref_prefix(), &n_pref,
+                         &n_items, keys, scratch);
+    __syncthreads();
+    ok = build_list(p, c, 1, chunk, ws + L.dec_order(), ws + L.dec_prefix(), &n_dec, &n_units,
+                    keys, scratch) && ok;
+    if (!ok) {
+      if (threadIdx.x == 0) atomicOr(&s_status, PVA_DEV_TOO_MANY);
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const uint32_t st = s_status;
+    SchedHeader h;
+    h.status = st;
+    h.n_pref = st ? 0 : n_pref;
+    h.n_items = st ? 0 : n_items;
+    h.n_dec = st ? 0 : n_dec;
+    h.n_units = st ? 0 : n_units;
+    h.tile_tokens = c.tile_tokens;
+    h.units_per_tile = c.units_per_tile;
+    h.dec_chunk = st ? 0 : s_chunk;
+    *hdr = h;
+    if (st) atomicOr(p.status, st);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_scheduler(const AttnParams& p, const SchedConfig& c, cudaStream_t s) {
+  pva_schedule_kernel<<<1, kThreads, 0, s>>>(p, c);
+  return cudaGetLastError();
+}
+
+}  // namespace pva

@@ -108,28 +108,39 @@ def cu_from_lengths(lengths) -> torch.Tensor:
 
 
 def make_packed(lq, lkv, H, Hkv, d, dv, dtype: str, sigma: float = 1.0, seed: int = 0,
-                gen: torch.Generator | None = None):
-    """Random packed Q/K/V (CPU tensors, ``dtype``) for given lengths."""
+                gen: torch.Generator | None = None, device: str = "cpu"):
+    """Random packed Q/K/V (tensors of ``dtype`` on ``device``) for given
+    lengths.  Values come from ``gen`` (or a generator on ``device`` seeded
+    with ``seed``); generation on a CUDA device uses that device's generator,
+    so its values differ from the CPU recipe but are just as reproducible."""
     if gen is None:
-        gen = torch.Generator("cpu")
+        gen = torch.Generator(device)
         gen.manual_seed(seed)
+    dev = gen.device
     tq, tkv = int(sum(lq)), int(sum(lkv))
     td = DTYPES[dtype]
-    q = (torch.randn((tq, H, d), generator=gen) * sigma).to(td)
-    k = (torch.randn((tkv, Hkv, d), generator=gen) * sigma).to(td)
-    v = (torch.randn((tkv, Hkv, dv), generator=gen) * sigma).to(td)
-    return q, k, v, cu_from_lengths(lq), cu_from_lengths(lkv)
+    q = (torch.randn((tq, H, d), generator=gen, device=dev) * sigma).to(td)
+    k = (torch.randn((tkv, Hkv, d), generator=gen, device=dev) * sigma).to(td)
+    v = (torch.randn((tkv, Hkv, dv), generator=gen, device=dev) * sigma).to(td)
+    return q, k, v, cu_from_lengths(lq).to(dev), cu_from_lengths(lkv).to(dev)
 
 
-def make(name: str, seed: int = 0, shrink: int = 1, B: int | None = None):
-    """Inputs for a named workload: dict with q, k, v, cu_q, cu_kv (CPU) and
-    the attention parameters."""
+def make(name: str, seed: int = 0, shrink: int = 1, B: int | None = None,
+         device: str = "cpu"):
+    """Inputs for a named workload: dict with q, k, v, cu_q, cu_kv and the
+    attention parameters.  Lengths always come from a CPU generator seeded
+    with ``seed``; on ``device='cpu'`` the values continue that generator's
+    stream, on a CUDA device they come from a generator on that device seeded
+    with ``seed + 1`` (used for the full-size workloads)."""
     w = WORKLOADS[name]
     if B is not None:
         w = Workload(**{**w.__dict__, "B": B})
     gen = torch.Generator("cpu")
     gen.manual_seed(seed)
     lq, lkv = draw_lengths(w, gen, shrink)
+    if device != "cpu":
+        gen = torch.Generator(device)
+        gen.manual_seed(seed + 1)
     q, k, v, cu_q, cu_kv = make_packed(lq, lkv, w.num_heads, w.kv_num_heads, w.head_size,
                                        w.v_head_size, w.dtype, w.sigma, gen=gen)
     return {
@@ -140,27 +151,3 @@ def make(name: str, seed: int = 0, shrink: int = 1, B: int | None = None):
         "dtype": w.dtype, "is_causal": w.is_causal, "scale": w.scale,
         "softcap": w.softcap, "sigma": w.sigma,
     }
-
-
-def unmasked_pairs(lq, lkv, is_causal: bool) -> int:
-    """Number of (query, key) pairs the mask leaves visible, summed over
-    sequences (per head).  Counting only, used for the FLOP figure."""
-    total = 0
-    for a, b in zip(lq, lkv):
-        a, b = int(a), int(b)
-        if not is_causal:
-            total += a * b
-            continue
-        off = b - a
-        # query i sees keys 0..min(b-1, i+off)
-        for_i_lo = max(0, -off)           # first row with any visible key
-        # rows with i + off >= b - 1 see all b keys
-        full_from = max(for_i_lo, b - 1 - off)
-        part_hi = min(a, full_from)
-        if part_hi > for_i_lo:
-            # sum_{i=lo}^{hi-1} (i + off + 1)
-            n = part_hi - for_i_lo
-            total += n * (off + 1) + (for_i_lo + part_hi - 1) * n // 2
-        if a > full_from:
-            total += (a - full_from) * b
-    return total

@@ -1,0 +1,149 @@
+/*
+ * pva.h -- packed variable-length attention (scaled dot-product attention
+ * over padding-free, variable-length sequences with MHA/GQA/MQA head
+ * sharing) for NVIDIA GB300 (sm_103a).  C ABI of libpva.so.
+ *
+ * The operation is the one defined on the "onnx-runtime-ep-cuda" source page
+ * packed_varlen_attention.rs (op `PackedVarlenAttention` v1):
+ *
+ *   - module doc "Packed layout & cumulative offsets": B sequences are
+ *     concatenated on one token axis; sequence b owns query rows
+ *     [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key/value rows
+ *     [cu_seqlens_kv[b], cu_seqlens_kv[b+1]); attention is block diagonal.
+ *   - "Schema (v1)": Q [total_q, num_heads, head_size], K [total_kv,
+ *     kv_num_heads, head_size], V [total_kv, kv_num_heads, v_head_size],
+ *     output [total_q, num_heads, v_head_size]; a rank-2 [tokens, heads*dim]
+ *     tensor has the same bytes.  kv_num_heads divides num_heads; query head h
+ *     reads key/value head h / (num_heads / kv_num_heads).
+ *   - "Causal alignment": with is_causal, local query i sees local key j iff
+ *     j <= i + (L_kv - L_q) (tail aligned).
+ *   - kernel stages 1-5: score = scale * q.k; with softcap != 0 the score is
+ *     replaced by softcap * tanh(score / softcap) before masking; softmax over
+ *     the visible keys; a row with no visible key is written as zeros;
+ *     out = sum_j p_j V[j].  Storage is f32, f16 or bf16 (codes 0, 1, 2, as on
+ *     the page); arithmetic is fp32; f16/bf16 outputs are rounded to nearest
+ *     even.
+ *
+ * All calls are asynchronous and stream ordered unless stated otherwise.
+ */
+#ifndef PVA_H
+#define PVA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes (negative = error; nothing was enqueued). */
+typedef enum {
+  PVA_OK = 0,
+  PVA_ERR_INVALID_ARG = -1, /* null pointer, bad count, bad dtype, non-finite scalar */
+  PVA_ERR_UNSUPPORTED = -2, /* valid request this build does not implement */
+  PVA_ERR_CUDA = -3,        /* a CUDA runtime call failed (see pva_last_error) */
+  PVA_ERR_OOM = -4          /* workspace allocation failed */
+} pva_status;
+
+/* Storage types of Q, K, V and the output (one type for all four). */
+typedef enum { PVA_F32 = 0, PVA_F16 = 1, PVA_BF16 = 2 } pva_dtype;
+
+/* Device-side status bits, latched by the on-device scheduler and read with
+ * pva_get_status.  When any bit is set the call wrote nothing to `out`. */
+#define PVA_DEV_CU_Q_START 0x1u   /* cu_seqlens_q[0] != 0 */
+#define PVA_DEV_CU_KV_START 0x2u  /* cu_seqlens_kv[0] != 0 */
+#define PVA_DEV_CU_Q_ORDER 0x4u   /* cu_seqlens_q decreases somewhere */
+#define PVA_DEV_CU_KV_ORDER 0x8u  /* cu_seqlens_kv decreases somewhere */
+#define PVA_DEV_TOO_MANY 0x10u    /* work count does not fit the 32-bit work index */
+#define PVA_DEV_WAIT_TIMEOUT 0x100u /* a pipeline wait in a kernel gave up (never expected) */
+
+/*
+ * pva_forward -- out = attention(q, k, v) over packed sequences.
+ *
+ * q, k, v, out : device pointers, row-major and contiguous, layouts as in
+ *                the schema above, all of storage type `dtype`.  For f16 and
+ *                bf16 each of q, k, v must be 16-byte aligned (tensor-memory
+ *                copies require it).  q, k, v are only read; out is only
+ *                written; out must not overlap q, k or v.
+ * cu_seqlens_q, cu_seqlens_kv : device pointers to int32 [B+1] cumulative
+ *                offsets, starting at 0 and non-decreasing.  cu_seqlens_q[B]
+ *                must equal total_q and cu_seqlens_kv[B] must equal total_kv
+ *                (the caller's contract: this signature carries no totals, and
+ *                the library never copies the offsets back to the host).
+ *                Violations of the start/order rules are detected on the
+ *                device: a status bit is latched, nothing is computed and
+ *                `out` is left untouched (see pva_get_status).
+ * B            : number of sequences, >= 1.  Empty sequences are allowed.
+ * num_heads, kv_num_heads : H >= 1 and Hkv >= 1 with H % Hkv == 0.
+ * head_size, v_head_size  : d and dv.  f16/bf16: d == dv in {64, 128, 256}
+ *                and H / Hkv <= 128.  f32: 1 <= d, dv <= 256.
+ * scale        : finite; 0 selects the default 1/sqrt(head_size) (computed in
+ *                fp32).  Any other value is used as given.
+ * is_causal    : nonzero selects the tail-aligned causal mask.
+ * softcap      : finite; 0 disables the cap; c and -c give the same result.
+ * dtype        : a pva_dtype code.
+ * stream       : cudaStream_t to enqueue on (0 = legacy default stream).
+ *
+ * Returns PVA_OK once the work is enqueued; it does not wait for it.  Memory:
+ * the library keeps one workspace per (device, stream), grown on demand
+ * inside this call (the growth synchronises `stream`); after the first call
+ * with the largest B, calls allocate nothing and never synchronise, so they
+ * can be captured into a CUDA graph.  Growth during stream capture returns
+ * PVA_ERR_INVALID_ARG.  Calls on one stream are ordered; calls on different
+ * streams use different workspaces.  Not re-entrant across host threads for
+ * the same stream.
+ */
+int pva_forward(const void* q, const void* k, const void* v,
+                const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                void* out, int B, int num_heads, int kv_num_heads,
+                int head_size, int v_head_size, float scale, int is_causal,
+                float softcap, int dtype, void* stream);
+
+/*
+ * pva_get_status -- synchronises `stream`, then reads and clears the device
+ * status bits (PVA_DEV_*) latched by the calls made on it since the last read.
+ * *device_flags receives 0 when every call was well formed.  Returns PVA_OK or
+ * PVA_ERR_CUDA (e.g. when no call has been made on this stream yet the flags
+ * are simply 0).
+ */
+int pva_get_status(void* stream, uint32_t* device_flags);
+
+/*
+ * pva_schedule -- runs only the on-device scheduler for the given offsets and
+ * copies its work description to host memory (synchronous; an inspection and
+ * test entry point).  `dtype` and the head/size arguments select the kernel
+ * family whose tiles are counted, exactly as pva_forward would.
+ *
+ * host_out receives int32 words:
+ *   [0] status bits, [1] n_prefill (sequences with prefill work),
+ *   [2] n_prefill_items, [3] n_decode (sequences routed to split-KV decode),
+ *   [4] n_decode_units, [5] q-tile rows in tokens, [6] units per q-tile,
+ *   [7] decode chunk in keys,
+ *   then B words: prefill sequence order (longest first; -1 padded),
+ *   then B+1 words: prefill item prefix sums in that order,
+ *   then B words: decode sequence order, then B+1 words: decode unit prefix.
+ * capacity is the number of int32 words host_out can hold (>= 8 + 4B + 2).
+ */
+int pva_schedule(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                 int B, int num_heads, int kv_num_heads, int head_size,
+                 int v_head_size, int is_causal, int dtype, int32_t* host_out,
+                 size_t capacity, void* stream);
+
+/* Human-readable text for a pva_status code (static storage). */
+const char* pva_status_string(int code);
+
+/* Text of the last error recorded by this host thread (static per thread). */
+const char* pva_last_error(void);
+
+/* Frees every workspace the library holds on the current device (waits for
+ * the streams that used them first). */
+void pva_release(void);
+
+/* Library version as (major << 16) | (minor << 8) | patch. */
+int pva_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PVA_H */

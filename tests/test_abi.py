@@ -1,0 +1,78 @@
+"""The C-ABI library builds, loads and exports every symbol include/*.h
+declares; host-side argument checks work without a GPU (CPU only)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import gqa_attention_cu_gb300 as pva
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pva.build()
+    return pva.load_library()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(pva_[a-z0-9_]+)\s*\(",
+                             text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("pva_forward", "pva_get_status", "pva_schedule", "pva_status_string",
+              "pva_last_error", "pva_release", "pva_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"libpva.so does not export {name}"
+
+
+def test_status_strings_and_version(lib):
+    assert pva.pva_status_string(0) == "ok"
+    assert "invalid" in pva.pva_status_string(-1)
+    assert "unsupported" in pva.pva_status_string(-2)
+    assert pva.pva_status_string(12345) == "unknown status"
+    assert pva.pva_version() == (0 << 16) | (1 << 8)
+
+
+def _call(lib, **kw):
+    args = dict(q=16, k=16, v=16, cq=16, ck=16, out=16, B=1, H=4, Hkv=2, d=128, dv=128,
+                scale=0.0, causal=0, softcap=0.0, dtype=2)
+    args.update(kw)
+    return lib.pva_forward(args["q"], args["k"], args["v"], args["cq"], args["ck"], args["out"],
+                           args["B"], args["H"], args["Hkv"], args["d"], args["dv"],
+                           args["scale"], args["causal"], args["softcap"], args["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(cq=None), -1), (dict(out=None), -1),
+    (dict(B=0), -1), (dict(H=0), -1), (dict(Hkv=0), -1), (dict(H=6, Hkv=4), -1),
+    (dict(dtype=3), -1), (dict(dtype=-1), -1),
+    (dict(scale=float("nan")), -1), (dict(softcap=float("inf")), -1),
+    (dict(d=96, dv=96), -2), (dict(d=128, dv=64), -2), (dict(dtype=0, d=512, dv=64), -2),
+    (dict(H=256, Hkv=1), -2), (dict(q=24), -1),
+])
+def test_host_argument_checks_need_no_gpu(lib, kw, code):
+    """Malformed calls are rejected on the host, before any CUDA call, with the
+    codes include/pva.h documents."""
+    assert _call(lib, **kw) == code
+    assert pva.pva_last_error() != ""
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(pva.PvaError):
+        pva.load_library(str(tmp_path / "missing.so"))
