@@ -1,0 +1,461 @@
+"""Benchmark of packed variable-length GQA attention on GB300.
+
+One step = one pva_forward (scheduler + prefill + decode kernels) over one
+packed batch of the named workload, inputs resident in HBM.  Default
+workload: bf16 causal GQA prefill, B=16, L_q=L_kv~U[128,2048], H=32, Hkv=8,
+d=dv=128 (metric: TFLOP/s counting only unmasked (q,k) pairs at 4*H*d FLOPs
+each).  The decode workload reports KV-read GB/s instead.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl reference]
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle (the only reference this build has) on a bounded sample of the same
+workload.  Under torchrun every rank runs its own batch (seed = rank): the
+work is independent per GPU (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD_TEXT = {
+    "bf16_prefill": "bf16 causal GQA prefill: B=16, L_q=L_kv~U[128,2048], H=32, Hkv=8, d=dv=128, "
+                    "default scale, softcap 0, N(0,1)",
+    "bf16_chunked": "bf16 tail-aligned causal chunked prefill: B=32, L_q~U[1,512], "
+                    "L_kv=L_q+U[0,4096], H=32, Hkv=8, d=128, N(0,1)",
+    "bf16_decode": "bf16 decode: B=256, L_q=1, L_kv~U[512,8192], H=32, Hkv=8, d=128, causal",
+    "bf16_longctx": "bf16 long-context MQA + softcap 50: B=4, L~logU[8192,32768], H=8, Hkv=1, "
+                    "d=dv=256, causal, N(0,2)",
+    "fp32_small": "fp32 non-causal: L={17,64,1,130}, H=Hkv=4, d=dv=64, scale 1/8",
+}
+METRIC = "varlen attn TFLOP/s (prefill) & KV-read GB/s (decode), % of roofline"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def unmasked_pairs(lq, lkv, is_causal: bool) -> int:
+    """(query, key) pairs the mask leaves visible, summed over sequences (one
+    head).  Query i of a sequence sees keys j <= i + L_kv - L_q when causal."""
+    total = 0
+    for a, b in zip(lq, lkv):
+        a, b = int(a), int(b)
+        if not is_causal:
+            total += a * b
+            continue
+        off = b - a
+        lo = max(0, -off)                # first row that sees any key
+        full = max(lo, b - 1 - off)      # rows from here on see all b keys
+        hi = min(a, full)
+        if hi > lo:
+            n = hi - lo
+            total += n * (off + 1) + (lo + hi - 1) * n // 2
+        if a > full:
+            total += (a - full) * b
+    return total
+
+
+def work_units(w):
+    """Algorithmic work of one step: (FLOPs, KV bytes)."""
+    pairs = unmasked_pairs(w["lq"], w["lkv"], w["is_causal"])
+    flops = pairs * 4 * w["num_heads"] * w["head_size"]
+    kv_bytes = sum(w["lkv"]) * w["kv_num_heads"] * (w["head_size"] + w["v_head_size"]) * \
+        (2 if w["dtype"] != "f32" else 4)
+    return flops, kv_bytes
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def recorded_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel_key)
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for src in rec.get("sources", []):
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec.get("sources_sha256"):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Largest per-rank value (step time) across the job; identity at N=1."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: int, world: int, device) -> int:
+    """Job-wide total of a per-rank count (work of independent batches)."""
+    if world <= 1:
+        return int(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([int(x)], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return int(t.item())
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class OracleSampler:
+    """Times the fp64 CPU oracle on bounded samples of a workload: sequences
+    of the workload's own length draw, materialised one at a time with the
+    same value recipe, and a uniform sample of their (token, head) output
+    rows.  Work is counted like the GPU arm's (visible pairs x 4 d FLOPs, or
+    K/V bytes for decode)."""
+
+    def __init__(self, w_name: str, seed: int = 0):
+        import numpy as np
+        import torch
+
+        from gqa_attention_cu_gb300 import workloads
+        self.np, self.torch, self.wl = np, torch, workloads
+        self.name = w_name
+        self.spec = workloads.WORKLOADS[w_name]
+        gen = torch.Generator("cpu").manual_seed(seed)
+        self.lq, self.lkv = workloads.draw_lengths(self.spec, gen)
+        self.rng = np.random.default_rng(seed + 7)
+        self.gen = torch.Generator("cpu").manual_seed(seed + 11)
+        self.per_pair = None
+
+    def _one(self, pair_budget: int):
+        np, sp = self.np, self.spec
+        import oracle
+        H, Hkv = sp.num_heads, sp.kv_num_heads
+        cand = [b for b in range(len(self.lq)) if self.lq[b] > 0]
+        b = int(self.rng.choice(cand))
+        lq, lkv = self.lq[b], self.lkv[b]
+        q, k, v, cq, ck = self.wl.make_packed([lq], [lkv], H, Hkv, sp.head_size, sp.v_head_size,
+                                              sp.dtype, sp.sigma, gen=self.gen)
+        i = np.arange(lq)
+        vis = np.minimum(lkv, i + (lkv - lq) + 1) if sp.is_causal else np.full(lq, lkv)
+        vis = np.maximum(vis, 0)
+        avg = max(1.0, float(vis.mean()))
+        n_rows = int(max(1, min(lq * H, pair_budget / avg)))
+        rows = np.sort(self.rng.choice(lq * H, size=n_rows, replace=False))
+        pairs = int(vis[rows // H].sum())
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, cq, ck, rows, H, Hkv, sp.scale, sp.is_causal, sp.softcap)
+        return time.perf_counter() - t0, pairs, n_rows
+
+    def run(self, seconds: float):
+        """Oracle work for about `seconds`; returns (seconds, pairs, rows)."""
+        if self.per_pair is None:
+            dt, pairs, _ = self._one(200_000)
+            self.per_pair = dt / max(pairs, 1)
+        tot_t = tot_p = tot_r = 0
+        while tot_t < seconds:
+            budget = max(10_000, int(min(seconds - tot_t, seconds / 2) / self.per_pair))
+            dt, pairs, n = self._one(budget)
+            tot_t, tot_p, tot_r = tot_t + dt, tot_p + pairs, tot_r + n
+        self.per_pair = tot_t / max(tot_p, 1)
+        return tot_t, tot_p, tot_r
+
+    def value(self, secs: float, pairs: int):
+        sp = self.spec
+        if self.name == "bf16_decode":
+            # every visible pair of a kv head's G query rows reads one K and V row;
+            # count each K/V row once per kv head, as the GPU arm does
+            kv = pairs / (sp.num_heads // sp.kv_num_heads) * (sp.head_size + sp.v_head_size) * 2
+            return kv / secs / 1e9, "GB/s"
+        return pairs * 4 * sp.head_size / secs / 1e12, "TFLOP/s"
+
+
+def run_reference(args, w_name):
+    """The fp64 CPU oracle, timed on the host cores, on a bounded sample of the
+    workload per step (rank 0 only; other ranks exit without work)."""
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    smp = OracleSampler(w_name)
+    for _ in range(args.warmup):
+        smp.run(args.ref_seconds / 4)
+    secs = pairs = rows = 0
+    for _ in range(args.steps):
+        t, p, r = smp.run(args.ref_seconds)
+        secs, pairs, rows = secs + t, pairs + p, rows + r
+    value, unit = smp.value(secs, pairs)
+    sample = (f"~{args.ref_seconds:g} s of oracle work per step: {rows // args.steps} random "
+              f"(token, head) output rows per step from sequences of the workload's length draw")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[w_name], "name": w_name, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w_name, seconds=12.0):
+    """The oracle as it stands on the host cores, on a bounded sample."""
+    import oracle
+    smp = OracleSampler(w_name)
+    secs, pairs, rows = smp.run(seconds)
+    value, unit = smp.value(secs, pairs)
+    return {"value": value, "unit": unit, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{rows} random (token, head) output rows from sequences of the "
+                      f"workload's length draw, {secs:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="bf16_prefill", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-seconds", type=float, default=4.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        run_reference(args, args.workload)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import gqa_attention_cu_gb300 as pva
+    from gqa_attention_cu_gb300 import workloads
+
+    rank, world, local = dist_info()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pva.build()
+    pva.load_library()
+
+    w_name = args.workload
+    w = workloads.make(w_name, seed=rank, device=str(dev))
+    H, Hkv, d, dv = w["num_heads"], w["kv_num_heads"], w["head_size"], w["v_head_size"]
+    flops, kv_bytes = work_units(w)
+    is_decode = w_name == "bf16_decode"
+    stream = torch.cuda.Stream(device=dev)
+    out = torch.empty(w["q"].shape[0], H, dv, dtype=w["q"].dtype, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(s):
+        pva.pva_forward(w["q"], w["k"], w["v"], w["cu_q"], w["cu_kv"], out, w["B"], H, Hkv, d,
+                        dv, w["scale"], int(w["is_causal"]), w["softcap"], stream=s)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step(stream)
+    torch.cuda.synchronize(dev)
+    if pva.pva_get_status(stream) != 0:
+        raise SystemExit("device status bits set during warm-up")
+
+    launches_per_step = 3 if w["dtype"] != "f32" and (H // Hkv) in (1, 2, 4, 8) else 2
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    kernel_ms = []
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    pva.pva_profile(True)
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)  # L2 flush: 256 MB write between steps
+            starts[i].record(stream)
+            step(stream)
+            ends[i].record(stream)
+            kernel_ms.append(pva.pva_kernel_times())
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    pva.pva_profile(False)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
+    job_flops = sum_over_ranks(flops, world, dev)
+    job_kv = sum_over_ranks(kv_bytes, world, dev)
+    if pva.pva_get_status(stream) != 0:
+        raise SystemExit("device status bits set during the timed steps")
+
+    # ---- end to end through the public API with host buffers ---------------
+    host = {k: w[k].cpu().pin_memory() for k in ("q", "k", "v", "cu_q", "cu_kv")}
+    dbuf = {k: torch.empty_like(w[k]) for k in host}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            flush.fill_(i & 0xff)
+            a.record(stream)
+            for k_ in host:
+                dbuf[k_].copy_(host[k_], non_blocking=True)
+            pva.pva_forward(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["cu_q"], dbuf["cu_kv"], out,
+                            w["B"], H, Hkv, d, dv, w["scale"], int(w["is_causal"]), w["softcap"],
+                            stream=stream)
+            out_host.copy_(out, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            if i >= args.warmup:
+                e2e_ms.append(a.elapsed_time(b))
+    e2e = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world, dev)
+
+    peaks = measured_peaks()
+    pre_ms = [k[1] for k in kernel_ms]
+    dec_ms = [k[2] for k in kernel_ms if k[2] >= 0]
+    if is_decode:
+        unit = "GB/s"
+        value = job_kv / (ms * 1e-3) / 1e9
+        e2e_v = job_kv / (e2e * 1e-3) / 1e9
+        dom_ms = sum(dec_ms) / len(dec_ms)
+        achieved = kv_bytes / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"],
+                "traffic": recorded_traffic("decode_bf16_d128_g4"),
+                "kernel": "pva_decode_kernel", "peak_source": peaks["source"] + " hbm_gbs"}
+    else:
+        unit = "TFLOP/s"
+        value = job_flops / (ms * 1e-3) / 1e12
+        e2e_v = job_flops / (e2e * 1e-3) / 1e12
+        dom_ms = sum(pre_ms) / len(pre_ms)
+        achieved = flops / (dom_ms * 1e-3) / 1e12
+        key = "bf16_tflops"
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks[key], "unit": "TFLOP/s",
+                "frac": achieved / peaks[key],
+                "traffic": recorded_traffic(f"prefill_{w_name}"),
+                "kernel": "pva_prefill_tc_kernel" if w["dtype"] != "f32" else "pva_prefill_f32_kernel",
+                "peak_source": peaks["source"] + " " + key + " (burst: kernel timed alone)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[w_name], "name": w_name,
+                   "l2": "flushed between steps (256 MB write); inputs also exceed L2"
+                   if not is_decode else "flushed between steps; K/V (4.6 GB) exceed L2",
+                   "tokens_q": int(w["cu_q"][-1]), "tokens_kv": int(w["cu_kv"][-1]),
+                   "flops_per_step": flops, "kv_bytes_per_step": kv_bytes,
+                   "kernel_ms": {"scheduler": sum(k[0] for k in kernel_ms) / len(kernel_ms),
+                                 "prefill": sum(pre_ms) / len(pre_ms),
+                                 "decode": (sum(dec_ms) / len(dec_ms)) if dec_ms else None},
+                   "parallelism": f"replicas x{world} (independent batches per GPU)"},
+        "roofline": roof,
+        "e2e": {"value": e2e_v, "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w_name)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

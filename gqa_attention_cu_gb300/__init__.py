@@ -16,8 +16,8 @@ import threading
 from . import workloads  # noqa: F401  (seeded synthetic inputs)
 
 __all__ = ["pva_forward", "pva_get_status", "pva_schedule", "pva_status_string",
-           "pva_last_error", "pva_release", "pva_version", "load_library", "build",
-           "PvaError", "DTYPE_CODES", "DEV_FLAGS"]
+           "pva_last_error", "pva_release", "pva_version", "pva_profile", "pva_kernel_times",
+           "pva_selftest_wait", "load_library", "build", "PvaError", "DTYPE_CODES", "DEV_FLAGS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpva.so")
@@ -70,6 +70,12 @@ def load_library(path: str | None = None):
         lib.pva_release.restype = None
         lib.pva_version.argtypes = []
         lib.pva_version.restype = i
+        lib.pva_profile.argtypes = [i]
+        lib.pva_profile.restype = i
+        lib.pva_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_float), i]
+        lib.pva_kernel_times.restype = i
+        lib.pva_selftest_wait.argtypes = [ctypes.c_uint32, vp, ctypes.POINTER(ctypes.c_uint32)]
+        lib.pva_selftest_wait.restype = i
         if path is None:
             _lib = lib
         return lib
@@ -147,3 +153,24 @@ def pva_release() -> None:
 
 def pva_version() -> int:
     return int(load_library().pva_version())
+
+
+def pva_selftest_wait(limit_us: int = 20000, stream=None) -> int:
+    """Run the bounded-wait self-test; returns the device bits it latched."""
+    lib = load_library()
+    flags = ctypes.c_uint32(0)
+    _check(lib.pva_selftest_wait(int(limit_us), _stream_ptr(stream), ctypes.byref(flags)))
+    return int(flags.value)
+
+
+def pva_profile(enable: bool) -> None:
+    """Bracket each later launch (this thread) with CUDA events (benchmarks)."""
+    _check(load_library().pva_profile(int(bool(enable))))
+
+
+def pva_kernel_times():
+    """Device durations (ms) of the last profiled call's launches:
+    (scheduler, prefill, decode or -1)."""
+    buf = (ctypes.c_float * 3)()
+    _check(load_library().pva_kernel_times(buf, 3))
+    return tuple(float(x) for x in buf)

@@ -24,6 +24,23 @@ namespace {
 
 thread_local std::string g_last_error;
 
+// Benchmark timing (pva_profile / pva_kernel_times): events around each launch.
+struct Profile {
+  bool enabled = false;
+  bool have = false;
+  bool decode = false;
+  int dev = -1;
+  cudaStream_t stream = nullptr;
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+};
+thread_local Profile g_prof;
+
+void prof_mark(int i, cudaStream_t s) {
+  if (!g_prof.enabled) return;
+  if (!g_prof.ev[i]) cudaEventCreate(&g_prof.ev[i]);
+  cudaEventRecord(g_prof.ev[i], s);
+}
+
 int fail(int code, const std::string& msg) {
   g_last_error = msg;
   return code;
@@ -134,7 +151,8 @@ int check_and_plan(const void* q, const void* k, const void* v, const int32_t* c
     if (mis & 15) return fail(PVA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
     plan->tensor_core = true;
     plan->decode = (G == 1 || G == 2 || G == 4 || G == 8);
-    plan->sched = SchedConfig{kTcRows / G, Hkv, tc_block_n(d), plan->decode ? 1 : 0, 0};
+    plan->sched = SchedConfig{(kTcRows / G) * tc_tiles_per_item(d), Hkv, tc_block_n(d),
+                              plan->decode ? 1 : 0, 0};
   }
   const WsLayout L{B, Hkv};
   plan->int_bytes = L.int_words() * 4;
@@ -263,18 +281,31 @@ int pva_forward(const void* q, const void* k, const void* v, const int32_t* cu_s
     }
   }
 
+  if (g_prof.enabled) {
+    g_prof.have = true;
+    g_prof.decode = plan.decode;
+    g_prof.stream = stream;
+    cudaGetDevice(&g_prof.dev);
+  }
+  prof_mark(0, stream);
   cudaError_t e = launch_scheduler(p, plan.sched, stream);
   if (e != cudaSuccess) return cuda_fail(e, "scheduler launch");
+  prof_mark(1, stream);
   if (!plan.tensor_core) {
     e = launch_prefill_f32(p, num_sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "fp32 attention launch");
+    prof_mark(2, stream);
     return PVA_OK;
   }
-  e = launch_prefill_tc(p, dtype, tq, tk, tv, num_sms, stream);
+  e = tc_tiles_per_item(head_size) == 2
+          ? launch_prefill_pair(p, dtype, tq, tk, tv, num_sms, stream)
+          : launch_prefill_tc(p, dtype, tq, tk, tv, num_sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
+  prof_mark(2, stream);
   if (plan.decode) {
     e = launch_decode(p, dtype, dk, dvm, num_sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "split-KV decode launch");
+    prof_mark(3, stream);
   }
   return PVA_OK;
 }
@@ -325,6 +356,46 @@ int pva_schedule(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int 
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
   e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  return PVA_OK;
+}
+
+int pva_selftest_wait(uint32_t limit_us, void* stream_, uint32_t* device_flags) {
+  if (!device_flags) return fail(PVA_ERR_INVALID_ARG, "device_flags is null");
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(PVA_ERR_INVALID_ARG, "limit_us must be in 1..1000000");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  uint32_t* dev = nullptr;
+  cudaError_t e = cudaMalloc(&dev, 16);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+  uint32_t host[2] = {0, 0};
+  e = cudaMemsetAsync(dev, 0, 16, stream);
+  if (e == cudaSuccess)
+    e = launch_wait_selftest(dev, (uint64_t)limit_us * 1000ull, reinterpret_cast<int*>(dev + 1),
+                             stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(host, dev, 8, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  cudaFree(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "wait self-test");
+  if (host[1] == 0) return fail(PVA_ERR_CUDA, "wait self-test kernel did not finish");
+  *device_flags = host[0];
+  return PVA_OK;
+}
+
+int pva_profile(int enable) {
+  g_prof.enabled = enable != 0;
+  g_prof.have = false;
+  return PVA_OK;
+}
+
+int pva_kernel_times(float* ms, int capacity) {
+  if (!ms || capacity < 3) return fail(PVA_ERR_INVALID_ARG, "need room for 3 durations");
+  if (!g_prof.have) return fail(PVA_ERR_INVALID_ARG, "no profiled call yet");
+  cudaError_t e = cudaStreamSynchronize(g_prof.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  ms[0] = ms[1] = ms[2] = -1.0f;
+  cudaEventElapsedTime(&ms[0], g_prof.ev[0], g_prof.ev[1]);
+  cudaEventElapsedTime(&ms[1], g_prof.ev[1], g_prof.ev[2]);
+  if (g_prof.decode) cudaEventElapsedTime(&ms[2], g_prof.ev[2], g_prof.ev[3]);
   return PVA_OK;
 }
 

@@ -107,6 +107,23 @@ __device__ __forceinline__ void load_dims(const uint8_t* row, int lane, float (&
   }
 }
 
+// G consecutive probabilities of one key (a broadcast shared-memory read).
+template <int G>
+__device__ __forceinline__ void load_probs(const float* src, float (&p)[G]) {
+  if constexpr (G >= 4) {
+#pragma unroll
+    for (int i = 0; i < G; i += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src + i);
+      p[i] = v.x; p[i + 1] = v.y; p[i + 2] = v.z; p[i + 3] = v.w;
+    }
+  } else if constexpr (G == 2) {
+    const float2 v = *reinterpret_cast<const float2*>(src);
+    p[0] = v.x; p[1] = v.y;
+  } else {
+    p[0] = src[0];
+  }
+}
+
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     pva_decode_kernel(AttnParams p, const __grid_constant__ CUtensorMap tmap_k,
@@ -173,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool capped = p.softcap != 0.0f;
     const float qmul = capped ? p.scale / p.softcap : p.scale * kLog2e;
     const float cap_mul = p.softcap * kLog2e;
-    const int my_r = lane / G, my_h = lane % G;  // pair owned after the reduce-scatter
+    const int my_r = lane / G;  // key of the (key, head) pair this lane owns after the reduce-scatter
     T* out = static_cast<T*>(p.out);
     uint32_t cnt = 0;
     bool ok = true;
@@ -264,12 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < R; ++r) {
             float vf[DPL];
             load_dims<T, DPL>(sV + (size_t)(r0 + r) * D * 2, lane, vf);
+            float pw[G];
+            load_probs<G>(sP + cw * 32 + r * G, pw);
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-              const float pw = sP[cw * 32 + r * G + hh];
+            for (int hh = 0; hh < G; ++hh)
 #pragma unroll
-              for (int e = 0; e < DPL; ++e) acc[hh][e] = fmaf(pw, vf[e], acc[hh][e]);
-            }
+              for (int e = 0; e < DPL; ++e) acc[hh][e] = fmaf(pw[hh], vf[e], acc[hh][e]);
           }
           __syncwarp();
         }

@@ -120,7 +120,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // it signals through *abort): sets the abort flag and the device status bit
 // and returns false.  Every pipeline wait in this library goes through here.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status) {
+                                          uint32_t* status,
+                                          uint64_t limit_ns = PVA_WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
@@ -128,7 +129,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_timer_ns() - t0 > PVA_WAIT_LIMIT_NS) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort = 1;
       atomicOr(status, PVA_DEV_WAIT_TIMEOUT);
       return false;

@@ -23,6 +23,9 @@ constexpr int kDecodeMaxSplits = 16;
 constexpr int kDecodeMaxGroup = 8;  // largest H/Hkv served by the split-KV decode kernel
 constexpr int kSortMax = 2048;      // sequences sorted on device; more keep input order
 
+// Query tiles per prefill work item: two 128-row tiles share each K/V tile
+// for d <= 128 (paired kernel); one tile for d = 256 (TMEM holds one 256-wide O).
+__host__ __device__ constexpr int tc_tiles_per_item(int D) { return D >= 256 ? 1 : 2; }
 // Keys per tensor-core key/value tile for head size D.
 __host__ __device__ constexpr int tc_block_n(int D) { return D >= 256 ? 64 : 128; }
 // Keys per decode key/value tile for head size D (16 KB of K per tile).
@@ -94,6 +97,10 @@ cudaError_t launch_prefill_f32(const AttnParams& p, int num_sms, cudaStream_t s)
 cudaError_t launch_prefill_tc(const AttnParams& p, int dtype, const CUtensorMap& tq,
                               const CUtensorMap& tk, const CUtensorMap& tv, int num_sms,
                               cudaStream_t s);
+cudaError_t launch_prefill_pair(const AttnParams& p, int dtype, const CUtensorMap& tq,
+                                const CUtensorMap& tk, const CUtensorMap& tv, int num_sms,
+                                cudaStream_t s);
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, int* done, cudaStream_t s);
 cudaError_t launch_decode(const AttnParams& p, int dtype, const CUtensorMap& tk,
                           const CUtensorMap& tv, int num_sms, cudaStream_t s);
 

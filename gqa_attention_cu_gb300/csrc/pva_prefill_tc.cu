@@ -39,7 +39,6 @@ namespace pva {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kSoftmaxWarp0 = 2;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows > 2^8
 
@@ -413,12 +412,6 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int dtype, const CUtensorMap&
                               cudaStream_t s) {
   const bool bf = dtype == PVA_BF16;
   switch (p.d) {
-    case 64:
-      return bf ? launch_tc<__nv_bfloat16, 64>(p, tq, tk, tv, num_sms, s)
-                : launch_tc<__half, 64>(p, tq, tk, tv, num_sms, s);
-    case 128:
-      return bf ? launch_tc<__nv_bfloat16, 128>(p, tq, tk, tv, num_sms, s)
-                : launch_tc<__half, 128>(p, tq, tk, tv, num_sms, s);
     case 256:
       return bf ? launch_tc<__nv_bfloat16, 256>(p, tq, tk, tv, num_sms, s)
                 : launch_tc<__half, 256>(p, tq, tk, tv, num_sms, s);

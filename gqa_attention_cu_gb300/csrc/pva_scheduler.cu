@@ -274,3 +274,36 @@ cudaError_t launch_scheduler(const AttnParams& p, const SchedConfig& c, cudaStre
 }
 
 }  // namespace pva
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded waits: one CTA waits on an mbarrier that nothing
+// ever completes, through the same helper every pipeline wait uses, with a
+// short limit.  The wait gives up, latches PVA_DEV_WAIT_TIMEOUT and the kernel
+// returns normally, leaving the context usable.
+// ---------------------------------------------------------------------------
+namespace pva {
+namespace {
+
+__global__ void pva_wait_selftest_kernel(uint32_t* status, uint64_t limit_ns, int* done) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // Nobody arrives on `bar`: every thread's wait must run out.
+  const bool ok = mbar_wait(&bar, 0, &abort_flag, status, limit_ns);
+  __syncthreads();
+  if (threadIdx.x == 0) *done = ok ? 1 : 2;
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, int* done, cudaStream_t s) {
+  pva_wait_selftest_kernel<<<1, 64, 0, s>>>(status, limit_ns, done);
+  return cudaGetLastError();
+}
+
+}  // namespace pva

@@ -129,6 +129,31 @@ int pva_schedule(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
                  int v_head_size, int is_causal, int dtype, int32_t* host_out,
                  size_t capacity, void* stream);
 
+/*
+ * Per-kernel timing for benchmarks.  pva_profile(1) makes every later
+ * pva_forward on this host thread bracket each kernel it launches with CUDA
+ * events recorded on the caller's stream (do not enable it while capturing a
+ * graph); pva_profile(0) turns it off.  pva_kernel_times synchronises the
+ * stream of the last profiled call and writes the device durations, in
+ * milliseconds, of its launches into ms[0..2]: [0] scheduler, [1] prefill
+ * kernel (tensor-core or fp32), [2] split-KV decode kernel (-1 when it was not
+ * launched).  Returns PVA_OK, or PVA_ERR_INVALID_ARG when no profiled call has
+ * been made.
+ */
+int pva_profile(int enable);
+int pva_kernel_times(float* ms, int capacity);
+
+/*
+ * pva_selftest_wait -- exercises the bounded waits that every kernel of this
+ * library uses on its pipeline barriers: one CTA waits on an mbarrier that
+ * nothing ever completes, with a limit of `limit_us` microseconds
+ * (1 .. 1000000).  The wait gives up, latches PVA_DEV_WAIT_TIMEOUT and the
+ * kernel returns; *device_flags receives the bits it latched.  Synchronous on
+ * `stream`; allocates and frees a few bytes of device memory.  Returns PVA_OK,
+ * PVA_ERR_INVALID_ARG (limit out of range) or PVA_ERR_CUDA.
+ */
+int pva_selftest_wait(uint32_t limit_us, void* stream, uint32_t* device_flags);
+
 /* Human-readable text for a pva_status code (static storage). */
 const char* pva_status_string(int code);
 

@@ -290,7 +290,7 @@ def sched_mirror(lq, lkv, H, Hkv, d, dtype, num_sms):
         tile, units, dec = 16, H, False
     else:
         G = H // Hkv
-        tile, units, dec = 128 // G, Hkv, G in (1, 2, 4, 8)
+        tile, units, dec = (128 // G) * (1 if d >= 256 else 2), Hkv, G in (1, 2, 4, 8)
     cap = min(B * Hkv * 16, 16384)
     INT_MAX = 2 ** 31 - 1
     chunk = INT_MAX
@@ -417,3 +417,18 @@ def test_full_size_workload_sampled_rows(name):
         full_index.append(tok * H + hh)
     got = out.view(-1, dv)[torch.tensor(full_index, device="cuda:0")]
     check(got, ref, "bf16")
+
+
+# ---------------------------------------------------------------------------
+# Failure detection: a bounded wait that nothing satisfies
+# ---------------------------------------------------------------------------
+def test_bounded_wait_gives_up_with_status_and_context_survives():
+    """The wait helper every pipeline barrier uses gives up after its limit,
+    latches the timeout bit and returns; the context stays usable."""
+    t0 = torch.cuda.Event(enable_timing=True)
+    flags = pva.pva_selftest_wait(20000)  # 20 ms
+    assert flags & pva.DEV_FLAGS["wait_timeout"]
+    # the device still computes correctly afterwards
+    parity([33, 5], [40, 5], 8, 2, 128, "bf16", causal=True, seed=41)
+    assert pva.pva_get_status() == 0
+    del t0
