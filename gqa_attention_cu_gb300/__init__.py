@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(_PKG, "libpva.so")
 PVA_OK, PVA_ERR_INVALID_ARG, PVA_ERR_UNSUPPORTED, PVA_ERR_CUDA, PVA_ERR_OOM = 0, -1, -2, -3, -4
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
 DEV_FLAGS = {"cu_q_start": 0x1, "cu_kv_start": 0x2, "cu_q_order": 0x4, "cu_kv_order": 0x8,
-             "too_many": 0x10, "wait_timeout": 0x100}
+             "too_many": 0x10, "null_tensor": 0x20, "wait_timeout": 0x100}
 
 _lock = threading.Lock()
 _lib = None

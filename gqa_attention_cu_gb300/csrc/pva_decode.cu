@@ -143,7 +143,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_abort, s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const SchedHeader h = *reinterpret_cast<const SchedHeader*>(p.ws + kWsHeader);
   uint32_t* status = p.status;
   volatile int* abort = &s_abort;
   const int total_kv = p.cu_kv[p.B];
@@ -157,6 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  wait_prior_grid();  // scheduler lists and the prefill kernel's writes are complete
+  const SchedHeader h = *reinterpret_cast<const SchedHeader*>(p.ws + kWsHeader);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -383,8 +384,7 @@ cudaError_t launch_dec(const AttnParams& p, const CUtensorMap& tk, const CUtenso
   auto kern = pva_decode_kernel<T, D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, kThreads, smem, s>>>(p, tk, tv);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(num_sms), dim3(kThreads), smem, s, p, tk, tv);
 }
 
 template <typename T, int D>

@@ -91,6 +91,25 @@ struct SchedConfig {
   int num_sms;
 };
 
+// Launches a kernel as a programmatic dependent of the previous work on the
+// stream: it may start (and run its set-up) while that work finishes, and
+// must execute griddepcontrol.wait before reading anything it produced.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // ---- launchers (defined next to their kernels) -------------------------------
 cudaError_t launch_scheduler(const AttnParams& p, const SchedConfig& c, cudaStream_t s);
 cudaError_t launch_prefill_f32(const AttnParams& p, int num_sms, cudaStream_t s);

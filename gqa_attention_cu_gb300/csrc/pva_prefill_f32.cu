@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(kWarps * 32) pva_prefill_f32_kernel(AttnParams
   float* sk = sq + kF32TileTokens * d;           // [32][d+1]
   float* sv = sk + kF32KeyTile * kstride;        // [32][dv]
 
+  wait_prior_grid();  // the scheduler's work lists are complete from here on
   const SchedHeader h = *reinterpret_cast<const SchedHeader*>(p.ws + kWsHeader);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float* Q = static_cast<const float*>(p.q);
@@ -140,8 +141,8 @@ cudaError_t launch_prefill_f32(const AttnParams& p, int num_sms, cudaStream_t s)
   cudaError_t e = cudaFuncSetAttribute(pva_prefill_f32_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  pva_prefill_f32_kernel<<<num_sms * 4, kWarps * 32, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(pva_prefill_f32_kernel, dim3(num_sms * 4), dim3(kWarps * 32), smem, s,
+                          p);
 }
 
 }  // namespace pva

@@ -6,20 +6,22 @@
 // work item covers 2m tokens (m = floor(128/G) tokens x G heads per tile), so
 // each K/V tile is loaded once for 256 MMA rows, and the tensor core
 // alternates between the two tiles: while softmax warpgroup 0 turns S0(j)
-// into P0(j), the tensor core computes P1(j-1)-side products and S1, and vice
-// versa.
+// into P0(j), the tensor core works on tile 1, and vice versa.
 //
 // Per CTA (persistent, one per SM, 320 threads):
 //   warp 0      TMA producer: the item's two Q tiles, then K_j and V_j into a
-//               ring of slots (K and V separately, so K_{j+1} can land while V_j
-//               is still being read).
+//               ring of slots (K and V separately, so K_{j+1} can land while
+//               V_j is still being read).
 //   warp 1      MMA issuer + TMEM owner.  Order per key tile j:
 //               PV0(j), S0(j+1), PV1(j), S1(j+1)  (S0(0), S1(0) up front).
 //   warps 2..5  softmax / correction / epilogue for query tile 0
 //   warps 6..9  the same for query tile 1
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+d), O1 after O0.
-// Shared memory (d = 128): Q0, Q1 32 KB each; 3 K/V slots of 32 KB; P0, P1
-// 32 KB each (16-bit probabilities in the 128-byte-swizzled K-major layout).
+// P_t (16-bit, two per column) overwrites the first 64 columns of S_t once
+// they have been read, and the P.V MMA takes its A operand from TMEM; the
+// next S_t MMA is issued after that P.V MMA (tcgen05 MMAs of one thread run in
+// issue order).  Shared memory (d = 128): Q0, Q1 32 KB each + 5 K/V slots of
+// 32 KB.
 #include "pva_device.cuh"
 #include "pva_items.cuh"
 
@@ -29,6 +31,7 @@ namespace {
 constexpr int kThreads = 320;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
+constexpr int kMaxSlots = 12;
 
 template <int D>
 struct PairCfg {
@@ -38,17 +41,15 @@ struct PairCfg {
   static constexpr int Q_TILE = KCH * Q_CHUNK;
   static constexpr int KV_CHUNK = BN * 128;           // 16 KB
   static constexpr int KV_TILE = KCH * KV_CHUNK;
-  static constexpr int SLOTS = D == 128 ? 3 : 6;
-  static constexpr int P_CHUNK = kTcRows * 128;
-  static constexpr int P_TILE = (BN / 64) * P_CHUNK;  // 32 KB
+  static constexpr int SLOTS = D == 128 ? 5 : 12;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = 2 * Q_TILE;
-  static constexpr int OFF_P = OFF_RING + SLOTS * KV_TILE;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_TILE;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static constexpr int OFF_BAR = OFF_RING + SLOTS * KV_TILE;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;   // barriers + alignment slack
   static constexpr int TMEM_COLS = 512;
   static constexpr int COL_S = 0;        // + 128 * tile
   static constexpr int COL_O = 256;      // + D * tile
+  static_assert(SLOTS <= kMaxSlots, "barrier array");
   static_assert(2 * BN + 2 * D <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448 - 64, "shared memory budget");
 };
@@ -56,8 +57,9 @@ struct PairCfg {
 struct PairBars {
   uint64_t q_full, q_empty, drain, pad;
   uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];
-  uint64_t ring_full[6], ring_empty[6];
+  uint64_t ring_full[kMaxSlots], ring_empty[kMaxSlots];
 };
+static_assert(sizeof(PairBars) <= 512, "barrier block");
 
 struct PairGeom {
   PrefillItem it;
@@ -91,11 +93,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const SchedHeader h = *reinterpret_cast<const SchedHeader*>(p.ws + kWsHeader);
   uint32_t* status = p.status;
   volatile int* abort = &s_abort;
   const int G = p.G;
-  const int m_tok = kTcRows / G;  // tokens per query tile (h.tile_tokens = 2 m)
+  const int m_tok = kTcRows / G;  // tokens per query tile (the item covers 2 m)
   const int total_q = p.cu_q[p.B];
   const int total_kv = p.cu_kv[p.B];
 
@@ -116,21 +117,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
   }
+  // Rows of the Q tiles beyond G*m are never written by the TMA unit; start
+  // them from zeros so no stale bits reach the MMA.
   for (int i = threadIdx.x; i < 2 * C::Q_TILE / 16; i += kThreads)
     reinterpret_cast<uint4*>(smem + C::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 1) tmem_alloc<C::TMEM_COLS>(&s_tmem_base);
+  if (warp == 0 && lane == 0) {
+    prefetch_tensor_map(&tmap_q);
+    prefetch_tensor_map(&tmap_k);
+    prefetch_tensor_map(&tmap_v);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem_base;
+  wait_prior_grid();  // the scheduler's work lists are complete from here on
+  allow_next_grid();
+  const SchedHeader h = *reinterpret_cast<const SchedHeader*>(p.ws + kWsHeader);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tensor_map(&tmap_q);
-      prefetch_tensor_map(&tmap_k);
-      prefetch_tensor_map(&tmap_v);
       uint32_t items = 0, loads = 0;
       const uint32_t q_bytes = 2u * C::KCH * (uint32_t)(G * m_tok) * 128u;
       bool ok = true;
@@ -164,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // Drain: every copy this thread issued must land before the CTA exits.
       if (items) mbar_wait(&bars->q_full, (items - 1) & 1, abort, status);
       for (int s = 0; s < C::SLOTS; ++s) {
         const uint32_t fills = loads > (uint32_t)s ? (loads - 1 - s) / C::SLOTS + 1 : 0;
@@ -177,7 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_o = idesc_f16<T>(kTcRows, D, false, true);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q);
       const uint32_t sRing = smem_u32(smem + C::OFF_RING);
-      const uint32_t sP = smem_u32(smem + C::OFF_P);
       uint32_t items = 0, loads = 0, tiles = 0;  // tiles: key tiles done (per query tile)
       bool ok = true;
       auto issue_s = [&](int t, uint32_t kslot) {
@@ -194,12 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars->s_full[t]);
       };
       auto issue_pv = [&](int t, uint32_t vslot, bool first) {
-        const uint32_t p_a = sP + t * C::P_TILE;
         const uint32_t v_a = sRing + vslot * C::KV_TILE;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ss(tmem + C::COL_O + t * D,
-                 sdesc_sw128(p_a + (kk >> 2) * C::P_CHUNK + (kk & 3) * 32, 16, 1024),
+          mma_ts(tmem + C::COL_O + t * D, tmem + C::COL_S + t * 128 + kk * 8,
                  sdesc_sw128(v_a + kk * 16 * 128, C::KV_CHUNK, 1024), idesc_o,
                  (!first || kk > 0) ? 1u : 0u);
         mma_commit(&bars->o_ready[t]);
@@ -251,23 +257,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tiles += n;
         ++items;
       }
+      // Drain: all issued MMAs complete before TMEM is released.
       mma_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, abort, status);
     }
   } else {
     // ------------------------------------------------- softmax + epilogue
     const int tq = warp >= 6 ? 1 : 0;  // query tile of this warpgroup
-    const int quarter = warp & 3;
+    const int quarter = warp & 3;      // TMEM lanes this warp may access
     const int r = quarter * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t col_s = C::COL_S + tq * 128, col_o = C::COL_O + tq * D;
-    uint8_t* sP = smem + C::OFF_P + tq * C::P_TILE;
     const float NEG_INF = __int_as_float(0xff800000);
     const bool capped = p.softcap != 0.0f;
     const float s_mul = capped ? p.scale / p.softcap : p.scale * kLog2e;
     const float cap_mul = p.softcap * kLog2e;
     const bool up = p.scale > 0.0f;  // direction of the (monotone) score transform
-    uint32_t tiles = 0, items = 0;
+    uint32_t tiles = 0;
     bool ok = true;
     T* out = static_cast<T*>(p.out);
 
@@ -308,13 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // transformed scores is the transform of this extreme.
         float ext = up ? NEG_INF : -NEG_INF;
 #pragma unroll
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(t_lane + col_s + c, v);
+        for (int c = 0; c < BN; c += 64) {
+          uint32_t va[32], vb[32];
+          tmem_ld32(t_lane + col_s + c, va);
+          tmem_ld32(t_lane + col_s + c + 32, vb);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float x = __uint_as_float(v[e]);
+          for (int e = 0; e < 64; ++e) {
+            float x = __uint_as_float(e < 32 ? va[e] : vb[e - 32]);
             if (!full_tile && (c + e < lo_c || c + e >= hi_c)) x = up ? NEG_INF : -NEG_INF;
             ext = up ? fmaxf(ext, x) : fminf(ext, x);
           }
@@ -325,13 +332,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_new = fmaxf(m_used, mt);
         float alpha = 1.0f;
         if (m_new > m_used + kRescaleThreshold) {
-          alpha = ex2_approx(m_used - m_new);
+          alpha = ex2_approx(m_used - m_new);  // 0 when m_used is -inf
           m_used = m_new;
         }
         const float m_eff = m_used == NEG_INF ? 0.0f : m_used;
         if (j > 0) {
-          // PV of the previous tile must be complete: it reads the P buffer
-          // about to be overwritten and accumulates into O.
+          // PV of the previous tile must be complete before O is rescaled.
           ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[tq], (T_ - 1) & 1, abort, status));
           if (!ok) break;
           tc_fence_after();
@@ -345,47 +351,51 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
               tmem_st32(t_lane + col_o + c, v);
             }
-            tmem_wait_st();
           }
         }
-        // Pass 2: p = 2^(x - m) per column, row sum, P (16-bit) -> shared
-        // memory, K-major 128-byte swizzle: 16-byte chunk q of row r of a
-        // 64-key half lands at chunk q ^ (r & 7).
+        // Pass 2: p = 2^(x - m), row sum, P (16-bit pairs) into TMEM over the
+        // S columns already read: columns [c, c+32) of S become P columns
+        // [c/2, c/2 + 16).
         float rs = 0.0f;
 #pragma unroll
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(t_lane + col_s + c, v);
+        for (int c = 0; c < BN; c += 64) {
+          uint32_t va[32], vb[32];
+          tmem_ld32(t_lane + col_s + c, va);
+          tmem_ld32(t_lane + col_s + c + 32, vb);
           tmem_wait_ld();
-          float pr[32];
+          uint32_t pw[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float sraw = __uint_as_float(v[e]);
-            float x = capped ? cap_mul * tanh_via_exp2(sraw * s_mul) - m_eff
-                             : fmaf(sraw, s_mul, -m_eff);
-            if (!full_tile && (c + e < lo_c || c + e >= hi_c)) x = NEG_INF;
-            pr[e] = ex2_approx(x);
-            rs += pr[e];
-          }
+          for (int e = 0; e < 64; e += 2) {
+            float pr[2];
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 w;
-            w.x = pack2<T>(pr[e + 0], pr[e + 1]);
-            w.y = pack2<T>(pr[e + 2], pr[e + 3]);
-            w.z = pack2<T>(pr[e + 4], pr[e + 5]);
-            w.w = pack2<T>(pr[e + 6], pr[e + 7]);
-            const int col = c + e, half = col >> 6, q16 = (col & 63) >> 3;
-            *reinterpret_cast<uint4*>(sP + half * C::P_CHUNK + r * 128 + ((q16 ^ (r & 7)) << 4)) =
-                w;
+            for (int u = 0; u < 2; ++u) {
+              const int cc = e + u;
+              const float sraw = __uint_as_float(cc < 32 ? va[cc] : vb[cc - 32]);
+              float x = capped ? cap_mul * tanh_via_exp2(sraw * s_mul) - m_eff
+                               : fmaf(sraw, s_mul, -m_eff);
+              if (!full_tile && (c + cc < lo_c || c + cc >= hi_c)) x = NEG_INF;
+              pr[u] = ex2_approx(x);
+              rs += pr[u];
+            }
+            pw[e >> 1] = pack2<T>(pr[0], pr[1]);
           }
+          uint32_t lo16[16], hi16[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            lo16[e] = pw[e];
+            hi16[e] = pw[16 + e];
+          }
+          tmem_st16(t_lane + col_s + (c >> 1), lo16);
+          tmem_st16(t_lane + col_s + (c >> 1) + 16, hi16);
         }
+        tmem_wait_st();
         l = l * alpha + rs;
-        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bars->p_full[tq]);
       }
       if (!ok) break;
 
+      // epilogue: O / l -> out (rows of this item only)
       const uint32_t T_last = tiles + n - 1;
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[tq], T_last & 1, abort, status));
       if (!ok) break;
@@ -411,7 +421,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->o_free[tq]);
       tiles += n;
-      ++items;
     }
   }
 
@@ -428,8 +437,7 @@ cudaError_t launch_pair(const AttnParams& p, const CUtensorMap& tq, const CUtens
   auto kern = pva_prefill_pair_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, kThreads, smem, s>>>(p, tq, tk, tv);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(num_sms), dim3(kThreads), smem, s, p, tq, tk, tv);
 }
 
 }  // namespace

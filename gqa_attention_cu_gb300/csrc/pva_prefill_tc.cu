@@ -107,11 +107,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const SchedHeader h = *reinterpret_cast<const SchedHeader*>(p.ws + kWsHeader);
   uint32_t* status = p.status;
   volatile int* abort = &s_abort;
   const int G = p.G;
-  const int m_tok = h.tile_tokens;
+  const int m_tok = kTcRows / G;  // tokens per query tile (one tile per item)
   const int total_q = p.cu_q[p.B];
   const int total_kv = p.cu_kv[p.B];
 
@@ -141,6 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem_base;
+  wait_prior_grid();  // the scheduler's work lists are complete from here on
+  allow_next_grid();
+  const SchedHeader h = *reinterpret_cast<const SchedHeader*>(p.ws + kWsHeader);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -401,8 +403,7 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tq, const CUtensor
   auto kern = pva_prefill_tc_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, kThreads, smem, s>>>(p, tq, tk, tv);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(num_sms), dim3(kThreads), smem, s, p, tq, tk, tv);
 }
 
 }  // namespace

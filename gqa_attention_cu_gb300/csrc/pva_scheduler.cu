@@ -66,12 +66,18 @@ struct SeqLens {
   int lq, lkv;
 };
 
-__device__ __forceinline__ SeqLens seq_lens(const AttnParams& p, int b) {
-  SeqLens s;
-  s.lq = p.cu_q[b + 1] - p.cu_q[b];
-  s.lkv = p.cu_kv[b + 1] - p.cu_kv[b];
-  return s;
-}
+// Per-sequence lengths: from shared memory when the batch was staged there
+// (B <= kSortMax: one coalesced pass over the offsets), else from global.
+struct Lengths {
+  const int32_t* cu_q;
+  const int32_t* cu_kv;
+  const int* s_lq;   // nullptr when not staged
+  const int* s_lkv;
+  __device__ __forceinline__ SeqLens operator()(int b) const {
+    if (s_lq) return SeqLens{s_lq[b], s_lkv[b]};
+    return SeqLens{cu_q[b + 1] - cu_q[b], cu_kv[b + 1] - cu_kv[b]};
+  }
+};
 
 __device__ __forceinline__ int decode_splits(int lkv, int chunk) {
   if (lkv <= chunk) return 1;
@@ -81,18 +87,18 @@ __device__ __forceinline__ int decode_splits(int lkv, int chunk) {
 
 // Builds one ordered list (class 0 = prefill, 1 = decode) and its prefix.
 // Returns false when the work count overflows int32.
-__device__ bool build_list(const AttnParams& p, const SchedConfig& c, int cls, int chunk,
-                           int32_t* order, int32_t* prefix, int* n_out, int* total_out,
-                           unsigned long long* keys, long long* scratch) {
+__device__ bool build_list(const AttnParams& p, const SchedConfig& c, const Lengths& seq_lens,
+                           int cls, int chunk, int32_t* order, int32_t* prefix, int* n_out,
+                           int* total_out, unsigned long long* keys, long long* scratch) {
   const int B = p.B;
   auto member = [&](int b) -> bool {
-    SeqLens s = seq_lens(p, b);
+    SeqLens s = seq_lens(b);
     if (s.lq <= 0) return false;
     const bool is_dec = c.decode_enabled && s.lq == 1;
     return cls == 1 ? is_dec : !is_dec;
   };
   auto work = [&](int b) -> long long {
-    SeqLens s = seq_lens(p, b);
+    SeqLens s = seq_lens(b);
     if (cls == 0)
       return (long long)((s.lq + c.tile_tokens - 1) / c.tile_tokens) * c.units_per_tile;
     return (long long)decode_splits(s.lkv, chunk) * p.Hkv;
@@ -105,7 +111,7 @@ __device__ bool build_list(const AttnParams& p, const SchedConfig& c, int cls, i
     for (int i = threadIdx.x; i < N; i += kThreads) {
       unsigned long long key = ~0ull;
       if (i < B && member(i)) {
-        SeqLens s = seq_lens(p, i);
+        SeqLens s = seq_lens(i);
         key = ((unsigned long long)(unsigned)(INT_MAX - s.lkv) << 32) | (unsigned)i;
       }
       keys[i] = key;
@@ -172,25 +178,41 @@ __device__ bool build_list(const AttnParams& p, const SchedConfig& c, int cls, i
 
 __global__ void __launch_bounds__(kThreads) pva_schedule_kernel(AttnParams p, SchedConfig c) {
   __shared__ unsigned long long keys[kSortMax];
+  __shared__ int s_lq[kSortMax], s_lkv[kSortMax];
   __shared__ long long scratch[32];
   __shared__ uint32_t s_status;
   __shared__ int s_chunk;
+
+  // The compute kernels are launched as programmatic dependents: let them
+  // start their set-up now; they wait for this grid before reading its output.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int B = p.B;
   const WsLayout L{B, p.Hkv};
   int32_t* ws = p.ws;
   SchedHeader* hdr = reinterpret_cast<SchedHeader*>(ws + kWsHeader);
+  const bool staged = B <= kSortMax;
+  const Lengths seq_lens{p.cu_q, p.cu_kv, staged ? s_lq : nullptr, staged ? s_lkv : nullptr};
 
   if (threadIdx.x == 0) {
     uint32_t st = 0;
     if (p.cu_q[0] != 0) st |= PVA_DEV_CU_Q_START;
     if (p.cu_kv[0] != 0) st |= PVA_DEV_CU_KV_START;
+    // Empty tensors may come as NULL; a NULL with a nonzero extent may not.
+    if ((!p.q || !p.out) && p.cu_q[B] != 0) st |= PVA_DEV_NULL_TENSOR;
+    if ((!p.k || !p.v) && p.cu_kv[B] != 0) st |= PVA_DEV_NULL_TENSOR;
     s_status = st;
   }
   __syncthreads();
   for (int b = threadIdx.x; b < B; b += kThreads) {
-    if (p.cu_q[b + 1] < p.cu_q[b]) atomicOr(&s_status, PVA_DEV_CU_Q_ORDER);
-    if (p.cu_kv[b + 1] < p.cu_kv[b]) atomicOr(&s_status, PVA_DEV_CU_KV_ORDER);
+    const int lq = p.cu_q[b + 1] - p.cu_q[b];
+    const int lkv = p.cu_kv[b + 1] - p.cu_kv[b];
+    if (lq < 0) atomicOr(&s_status, PVA_DEV_CU_Q_ORDER);
+    if (lkv < 0) atomicOr(&s_status, PVA_DEV_CU_KV_ORDER);
+    if (staged) {
+      s_lq[b] = lq;
+      s_lkv[b] = lkv;
+    }
   }
   // Completion counters of the decode combine start at zero every call.
   int32_t* done = ws + L.dec_done();
@@ -204,7 +226,7 @@ __global__ void __launch_bounds__(kThreads) pva_schedule_kernel(AttnParams p, Sc
     if (c.decode_enabled) {
       long long keyrows = 0, cnt = 0;
       for (int b = threadIdx.x; b < B; b += kThreads) {
-        SeqLens s = seq_lens(p, b);
+        SeqLens s = seq_lens(b);
         if (s.lq == 1) {
           keyrows += s.lkv;
           cnt += 1;
@@ -221,7 +243,7 @@ __global__ void __launch_bounds__(kThreads) pva_schedule_kernel(AttnParams p, Sc
         long long units = 0;
         int any_split = 0;
         for (int b = threadIdx.x; b < B; b += kThreads) {
-          SeqLens s = seq_lens(p, b);
+          SeqLens s = seq_lens(b);
           if (s.lq == 1) {
             int sp = decode_splits(s.lkv, chunk > INT_MAX ? INT_MAX : (int)chunk);
             units += (long long)sp * p.Hkv;
@@ -240,11 +262,11 @@ __global__ void __launch_bounds__(kThreads) pva_schedule_kernel(AttnParams p, Sc
     }
     __syncthreads();
     const int chunk = s_chunk;
-    bool ok = build_list(p, c, 0, chunk, ws + L.pref_order(), ws + L.pref_prefix(), &n_pref,
-                         &n_items, keys, scratch);
+    bool ok = build_list(p, c, seq_lens, 0, chunk, ws + L.pref_order(), ws + L.pref_prefix(),
+                         &n_pref, &n_items, keys, scratch);
     __syncthreads();
-    ok = build_list(p, c, 1, chunk, ws + L.dec_order(), ws + L.dec_prefix(), &n_dec, &n_units,
-                    keys, scratch) && ok;
+    ok = build_list(p, c, seq_lens, 1, chunk, ws + L.dec_order(), ws + L.dec_prefix(), &n_dec,
+                    &n_units, keys, scratch) && ok;
     if (!ok) {
       if (threadIdx.x == 0) atomicOr(&s_status, PVA_DEV_TOO_MANY);
     }

@@ -55,6 +55,7 @@ typedef enum { PVA_F32 = 0, PVA_F16 = 1, PVA_BF16 = 2 } pva_dtype;
 #define PVA_DEV_CU_Q_ORDER 0x4u   /* cu_seqlens_q decreases somewhere */
 #define PVA_DEV_CU_KV_ORDER 0x8u  /* cu_seqlens_kv decreases somewhere */
 #define PVA_DEV_TOO_MANY 0x10u    /* work count does not fit the 32-bit work index */
+#define PVA_DEV_NULL_TENSOR 0x20u /* a NULL q/k/v/out with a nonzero token extent */
 #define PVA_DEV_WAIT_TIMEOUT 0x100u /* a pipeline wait in a kernel gave up (never expected) */
 
 /*
@@ -62,9 +63,12 @@ typedef enum { PVA_F32 = 0, PVA_F16 = 1, PVA_BF16 = 2 } pva_dtype;
  *
  * q, k, v, out : device pointers, row-major and contiguous, layouts as in
  *                the schema above, all of storage type `dtype`.  For f16 and
- *                bf16 each of q, k, v must be 16-byte aligned (tensor-memory
+ *                bf16 each of q, k, v, out must be 16-byte aligned (tensor
  *                copies require it).  q, k, v are only read; out is only
- *                written; out must not overlap q, k or v.
+ *                written; out must not overlap q, k or v.  q and out may be
+ *                NULL when total_q is 0, k and v when total_kv is 0 (an empty
+ *                tensor); a NULL pointer with a nonzero extent is caught on the
+ *                device (PVA_DEV_NULL_TENSOR, nothing computed).
  * cu_seqlens_q, cu_seqlens_kv : device pointers to int32 [B+1] cumulative
  *                offsets, starting at 0 and non-decreasing.  cu_seqlens_q[B]
  *                must equal total_q and cu_seqlens_kv[B] must equal total_kv

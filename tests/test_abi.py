@@ -59,7 +59,7 @@ def _call(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(q=None), -1), (dict(cq=None), -1), (dict(out=None), -1),
+    (dict(cq=None), -1), (dict(ck=None), -1),
     (dict(B=0), -1), (dict(H=0), -1), (dict(Hkv=0), -1), (dict(H=6, Hkv=4), -1),
     (dict(dtype=3), -1), (dict(dtype=-1), -1),
     (dict(scale=float("nan")), -1), (dict(softcap=float("inf")), -1),

@@ -128,8 +128,11 @@ def test_empty_and_degenerate_sequences(dtype):
 
 
 def test_all_sequences_empty_writes_nothing():
+    """total_q = 0: an empty Q tensor (null data pointer) is accepted, nothing
+    is written."""
     dev = torch.device("cuda:0")
     q = torch.zeros(0, 4, 128, dtype=torch.bfloat16, device=dev)
+    assert q.data_ptr() == 0
     k = torch.randn(10, 2, 128, device=dev).to(torch.bfloat16)
     v = torch.randn(10, 2, 128, device=dev).to(torch.bfloat16)
     cq = torch.tensor([0, 0, 0], dtype=torch.int32, device=dev)
@@ -138,6 +141,26 @@ def test_all_sequences_empty_writes_nothing():
     pva.pva_forward(q, k, v, cq, ck, canary, 2, 4, 2, 128, 128, 0.0, 1, 0.0)
     assert pva.pva_get_status() == 0
     assert torch.all(canary == 7.0)
+    empty_out = torch.empty(0, 4, 128, dtype=torch.bfloat16, device=dev)
+    pva.pva_forward(q, k, v, cq, ck, empty_out, 2, 4, 2, 128, 128, 0.0, 1, 0.0)
+    assert pva.pva_get_status() == 0
+
+
+def test_null_tensor_with_nonzero_extent_latches_status():
+    """A null Q with cu_seqlens_q[B] > 0 is caught on the device: status bit,
+    nothing computed."""
+    dev = torch.device("cuda:0")
+    k = torch.randn(10, 2, 128, device=dev).to(torch.bfloat16)
+    cq = torch.tensor([0, 3], dtype=torch.int32, device=dev)
+    ck = torch.tensor([0, 10], dtype=torch.int32, device=dev)
+    out = torch.full((3, 4, 128), 5.0, dtype=torch.bfloat16, device=dev)
+    lib = pva.load_library()
+    rc = lib.pva_forward(None, k.data_ptr(), k.data_ptr(), cq.data_ptr(), ck.data_ptr(),
+                         out.data_ptr(), 1, 4, 2, 128, 128, 0.0, 1, 0.0, 2,
+                         torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    assert pva.pva_get_status() & pva.DEV_FLAGS["null_tensor"]
+    assert torch.all(out == 5.0)
 
 
 def test_single_short_batch_smaller_than_a_tile():
@@ -268,9 +291,9 @@ def test_malformed_offsets_latch_status_and_write_nothing(bad):
     elif bad == "kv_start":
         ck[0] = 2
     elif bad == "q_order":
-        cq[1] = 25
+        cq[1] = 35   # [0, 35, 30]: decreases
     else:
-        ck[1] = 25
+        ck[1] = 35
     out = torch.full((30, 4, 128), 5.0, dtype=torch.bfloat16, device=dev)
     pva.pva_forward(q.to(dev), k.to(dev), v.to(dev), cq.to(dev), ck.to(dev), out, 2, 4, 2, 128,
                     128, 0.0, 1, 0.0)
