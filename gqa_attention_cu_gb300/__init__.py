@@ -76,6 +76,9 @@ def load_library(path: str | None = None):
         lib.pva_kernel_times.restype = i
         lib.pva_selftest_wait.argtypes = [ctypes.c_uint32, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.pva_selftest_wait.restype = i
+        lib.pva_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, f, i,
+                                            vp, vp]
+        lib.pva_forward_noalloc.restype = i
         if path is None:
             _lib = lib
         return lib
@@ -116,6 +119,26 @@ def pva_forward(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B: int, num_heads: in
                          cu_seqlens_kv.data_ptr(), out.data_ptr(), int(B), int(num_heads),
                          int(kv_num_heads), int(head_size), int(v_head_size), float(scale),
                          int(is_causal), float(softcap), code, _stream_ptr(stream))
+    _check(rc)
+
+
+def pva_forward_noalloc(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B: int, num_heads: int,
+                        kv_num_heads: int, head_size: int, v_head_size: int, scale: float = 0.0,
+                        is_causal: int = 0, softcap: float = 0.0, dtype: int | None = None,
+                        device_status=None, stream=None) -> None:
+    """pva_forward for callers that cannot allocate device memory at call
+    time: the library uses its fixed 4 MiB per-device scratch array instead of
+    a per-stream workspace (see include/pva.h for the limits and the rule that
+    overlapping calls race).  ``device_status`` is an optional CUDA uint32
+    tensor the call ORs its status bits into."""
+    lib = load_library()
+    code = _dtype_code(q) if dtype is None else int(dtype)
+    st = device_status.data_ptr() if device_status is not None else None
+    rc = lib.pva_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                 cu_seqlens_q.data_ptr(), cu_seqlens_kv.data_ptr(),
+                                 out.data_ptr(), int(B), int(num_heads), int(kv_num_heads),
+                                 int(head_size), int(v_head_size), float(scale), int(is_causal),
+                                 float(softcap), code, st, _stream_ptr(stream))
     _check(rc)
 
 

@@ -20,7 +20,8 @@
 
 using namespace pva;
 
-namespace {
+namespace pva {
+namespace host {
 
 thread_local std::string g_last_error;
 
@@ -114,14 +115,6 @@ int encode_map(CUtensorMap* map, const void* base, int dtype, int dim, int heads
   return PVA_OK;
 }
 
-struct Plan {
-  bool tensor_core = false;  // bf16/f16 tcgen05 prefill
-  bool decode = false;       // split-KV decode kernel for L_q == 1
-  SchedConfig sched{};
-  size_t int_bytes = 0, partial_bytes = 0;
-  int cap_units = 0;
-};
-
 int check_and_plan(const void* q, const void* k, const void* v, const int32_t* cu_q,
                    const int32_t* cu_kv, void* out, int B, int H, int Hkv, int d, int dv,
                    float scale, float softcap, int dtype, Plan* plan) {
@@ -166,6 +159,13 @@ int check_and_plan(const void* q, const void* k, const void* v, const int32_t* c
   }
   return PVA_OK;
 }
+
+}  // namespace host
+}  // namespace pva
+
+using namespace pva::host;
+
+namespace {
 
 int get_workspace(int dev, cudaStream_t stream, size_t need, Workspace** out) {
   Workspace& w = g_ws[{dev, stream}];

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string>
 #include <type_traits>
 
 #include "pva.h"
@@ -90,6 +91,26 @@ struct SchedConfig {
   int decode_enabled;  // route L_q == 1 sequences to the decode kernel
   int num_sms;
 };
+
+// ---- host helpers shared by the entry points (pva_api.cu) --------------------
+namespace host {
+// Validated launch plan of one call.
+struct Plan {
+  bool tensor_core = false;  // bf16/f16 tcgen05 prefill
+  bool decode = false;       // split-KV decode kernel for L_q == 1
+  SchedConfig sched{};
+  size_t int_bytes = 0, partial_bytes = 0;
+  int cap_units = 0;
+};
+int fail(int code, const std::string& msg);
+int cuda_fail(cudaError_t e, const char* what);
+int get_encoder();
+int encode_map(CUtensorMap* map, const void* base, int dtype, int dim, int heads, int box_dim,
+               int box_heads, int box_tokens, bool swizzle128);
+int check_and_plan(const void* q, const void* k, const void* v, const int32_t* cu_q,
+                   const int32_t* cu_kv, void* out, int B, int H, int Hkv, int d, int dv,
+                   float scale, float softcap, int dtype, Plan* plan);
+}  // namespace host
 
 // Launches a kernel as a programmatic dependent of the previous work on the
 // stream: it may start (and run its set-up) while that work finishes, and

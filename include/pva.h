@@ -104,6 +104,36 @@ int pva_forward(const void* q, const void* k, const void* v,
                 float softcap, int dtype, void* stream);
 
 /*
+ * pva_forward_noalloc -- the same attention as pva_forward, for callers that
+ * cannot allocate device memory when they call (a runtime whose device memory
+ * is planned ahead and owned by an arena or governor, code that runs while
+ * another component holds the allocator, a process with a fixed device
+ * footprint).  The pages have no counterpart of this entry point.
+ *
+ * It calls no cudaMalloc, cudaFree or allocating library routine: its scratch
+ * (work lists, decode split partials and counters, a status word) is one
+ * file-scope device array of 4 MiB that every GPU loading the library holds
+ * until the process exits.  Arguments are those of pva_forward, plus:
+ *   device_status : optional device pointer to a uint32 the call ORs its
+ *                   PVA_DEV_* bits into (the caller clears it); NULL uses a
+ *                   word inside the scratch, which each call clears first.
+ * Limits: B * (4 + kv_num_heads) int32 words of work lists must fit in 1 MiB
+ * (else PVA_ERR_UNSUPPORTED with nothing enqueued); decode splits are limited
+ * to the partials that fit in the rest of the array.  All calls on a device
+ * share the array: calls whose kernels overlap on the GPU race and give wrong
+ * results, so keep them ordered (one stream, or events between streams).  The
+ * array keeps the last call's contents; what must start at zero is cleared
+ * by each call.  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress with that device current); make it before any
+ * stream capture.
+ */
+int pva_forward_noalloc(const void* q, const void* k, const void* v,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                        void* out, int B, int num_heads, int kv_num_heads,
+                        int head_size, int v_head_size, float scale, int is_causal,
+                        float softcap, int dtype, uint32_t* device_status, void* stream);
+
+/*
  * pva_get_status -- synchronises `stream`, then reads and clears the device
  * status bits (PVA_DEV_*) latched by the calls made on it since the last read.
  * *device_flags receives 0 when every call was well formed.  Returns PVA_OK or
