@@ -9,9 +9,10 @@
 // into P0(j), the tensor core works on tile 1, and vice versa.
 //
 // Per CTA (persistent, one per SM, 320 threads):
-//   warp 0      TMA producer: the item's two Q tiles, then K_j and V_j into a
-//               ring of slots (K and V separately, so K_{j+1} can land while
-//               V_j is still being read).
+//   warp 0      TMA producer.  Decodes each work item once and publishes it
+//               to the other roles through a small shared-memory ring, then
+//               loads the item's two Q tiles and K_j, V_j into a ring of slots
+//               (K and V separately, so K_{j+1} can land while V_j is read).
 //   warp 1      MMA issuer + TMEM owner.  Order per key tile j:
 //               PV0(j), S0(j+1), PV1(j), S1(j+1)  (S0(0), S1(0) up front).
 //   warps 2..5  softmax / correction / epilogue for query tile 0
@@ -22,6 +23,13 @@
 // next S_t MMA is issued after that P.V MMA (tcgen05 MMAs of one thread run in
 // issue order).  Shared memory (d = 128): Q0, Q1 32 KB each + 5 K/V slots of
 // 32 KB.
+//
+// The softmax loops are specialised so that no uniform decision is taken per
+// element: softcap on/off is a template parameter, and "tile needs a mask" and
+// the sign of the scale are decided once per tile.  Pass 1 takes the row
+// extreme of the raw scores with three-input max/min; pass 2 forms
+// x*scale*log2(e) - m with packed fp32x2 FMAs, exponentiates with ex2 and
+// sums with packed adds.
 #include "pva_device.cuh"
 #include "pva_items.cuh"
 
@@ -32,6 +40,8 @@ constexpr int kThreads = 320;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kMaxSlots = 12;
+constexpr int kItemSlots = 4;
+constexpr int kSoftmaxWarps = 8;
 
 template <int D>
 struct PairCfg {
@@ -45,7 +55,7 @@ struct PairCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = 2 * Q_TILE;
   static constexpr int OFF_BAR = OFF_RING + SLOTS * KV_TILE;
-  static constexpr int SMEM = OFF_BAR + 512 + 1024;   // barriers + alignment slack
+  static constexpr int SMEM = OFF_BAR + 1024 + 1024;  // barriers/item ring + alignment slack
   static constexpr int TMEM_COLS = 512;
   static constexpr int COL_S = 0;        // + 128 * tile
   static constexpr int COL_O = 256;      // + D * tile
@@ -54,31 +64,76 @@ struct PairCfg {
   static_assert(SMEM <= 232448 - 64, "shared memory budget");
 };
 
+// A decoded work item, as the producer publishes it.
+struct ItemSlot {
+  int q_start, kv_start, lq, lkv;
+  int t, unit, n_tiles, q0;
+  int last;  // 1: no more items for this CTA
+  int pad[3];
+};
+
 struct PairBars {
   uint64_t q_full, q_empty, drain, pad;
   uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];
   uint64_t ring_full[kMaxSlots], ring_empty[kMaxSlots];
+  uint64_t item_full[kItemSlots], item_empty[kItemSlots];
+  ItemSlot items[kItemSlots];
 };
-static_assert(sizeof(PairBars) <= 512, "barrier block");
+static_assert(sizeof(PairBars) <= 1024, "barrier block");
 
-struct PairGeom {
-  PrefillItem it;
-  int n_tiles;  // key tiles (both query tiles visit the same ones)
-  int q0;       // packed token of row-group 0 of query tile 0 (tile 1 = q0 + m)
-};
-
-__device__ __forceinline__ PairGeom pair_geom(const AttnParams& p, const SchedHeader& h, int idx,
-                                              int total_q, int m) {
-  PairGeom g;
-  g.it = decode_prefill_item(p, h, idx);
-  const int hi = item_key_extent(g.it, h.tile_tokens, p.is_causal);
-  g.n_tiles = (hi + 127) / 128;
-  const int want = g.it.q_start + g.it.t * h.tile_tokens;
-  g.q0 = min(want, total_q - 2 * m);
-  return g;
+// ---- softmax building blocks (64 columns at a time) --------------------------
+__device__ __forceinline__ float col_val(const uint32_t (&va)[32], const uint32_t (&vb)[32],
+                                         int e) {
+  return __uint_as_float(e < 32 ? va[e] : vb[e - 32]);
 }
 
-template <typename T, int D>
+// Extreme (max if UP, else min) of the raw scores of columns [c, c+64);
+// MASKED replaces the columns outside [lo_c, hi_c) by the neutral value.
+template <bool UP, bool MASKED>
+__device__ __forceinline__ float extreme64(const uint32_t (&va)[32], const uint32_t (&vb)[32],
+                                           int c, int lo_c, int hi_c, float ext) {
+  const float neutral = UP ? __int_as_float(0xff800000) : __int_as_float(0x7f800000);
+#pragma unroll
+  for (int e = 0; e < 64; e += 2) {
+    float x0 = col_val(va, vb, e), x1 = col_val(va, vb, e + 1);
+    if (MASKED) {
+      x0 = (c + e >= lo_c && c + e < hi_c) ? x0 : neutral;
+      x1 = (c + e + 1 >= lo_c && c + e + 1 < hi_c) ? x1 : neutral;
+    }
+    ext = UP ? fmax3f(ext, x0, x1) : fmin3f(ext, x0, x1);
+  }
+  return ext;
+}
+
+// p = 2^(x - m) for columns [c, c+64), x the transformed score; row sums in
+// rs; p packed as 16-bit pairs into pw.
+template <typename T, bool CAP, bool MASKED>
+__device__ __forceinline__ void exp64(const uint32_t (&va)[32], const uint32_t (&vb)[32], int c,
+                                      int lo_c, int hi_c, float s_mul, float cap_mul, float m_eff,
+                                      float2& rs, uint32_t (&pw)[32]) {
+  const float2 mul2 = make_float2(s_mul, s_mul), neg_m = make_float2(-m_eff, -m_eff);
+#pragma unroll
+  for (int e = 0; e < 64; e += 2) {
+    const float2 s = make_float2(col_val(va, vb, e), col_val(va, vb, e + 1));
+    float2 x;
+    if (CAP) {
+      x.x = cap_mul * tanh_via_exp2(s.x * s_mul) - m_eff;
+      x.y = cap_mul * tanh_via_exp2(s.y * s_mul) - m_eff;
+    } else {
+      x = ffma2(s, mul2, neg_m);
+    }
+    if (MASKED) {
+      const float ninf = __int_as_float(0xff800000);
+      x.x = (c + e >= lo_c && c + e < hi_c) ? x.x : ninf;
+      x.y = (c + e + 1 >= lo_c && c + e + 1 < hi_c) ? x.y : ninf;
+    }
+    const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    rs = fadd2(rs, p);
+    pw[e >> 1] = pack2<T>(p.x, p.y);
+  }
+}
+
+template <typename T, int D, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     pva_prefill_pair_kernel(AttnParams p, const __grid_constant__ CUtensorMap tmap_q,
                             const __grid_constant__ CUtensorMap tmap_k,
@@ -115,6 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->ring_full[s], 1);
       mbar_init(&bars->ring_empty[s], 1);
     }
+    for (int s = 0; s < kItemSlots; ++s) {
+      mbar_init(&bars->item_full[s], 1);
+      mbar_init(&bars->item_empty[s], 1 + kSoftmaxWarps);  // MMA thread + one lane per warp
+    }
     fence_mbar_init();
   }
   // Rows of the Q tiles beyond G*m are never written by the TMA unit; start
@@ -134,18 +193,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s_tmem_base;
   wait_prior_grid();  // the scheduler's work lists are complete from here on
   allow_next_grid();
-  const SchedHeader h = *reinterpret_cast<const SchedHeader*>(p.ws + kWsHeader);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t items = 0, loads = 0;
+      const SchedHeader h = *reinterpret_cast<const SchedHeader*>(p.ws + kWsHeader);
+      uint32_t items = 0, loads = 0, published = 0;
       const uint32_t q_bytes = 2u * C::KCH * (uint32_t)(G * m_tok) * 128u;
       bool ok = true;
+      auto publish = [&](const ItemSlot& v) -> bool {
+        const int sl = published % kItemSlots;
+        if (!mbar_wait(&bars->item_empty[sl], ((published / kItemSlots) & 1) ^ 1, abort, status))
+          return false;
+        bars->items[sl] = v;
+        mbar_arrive(&bars->item_full[sl]);
+        ++published;
+        return true;
+      };
       for (int idx = blockIdx.x; ok && idx < h.n_items; idx += gridDim.x) {
-        const PairGeom pg = pair_geom(p, h, idx, total_q, m_tok);
-        if (pg.n_tiles == 0) continue;
-        const int g = pg.it.unit;
+        const PrefillItem it = decode_prefill_item(p, h, idx);
+        const int hi = item_key_extent(it, h.tile_tokens, p.is_causal);
+        ItemSlot v;
+        v.q_start = it.q_start;
+        v.kv_start = it.kv_start;
+        v.lq = it.lq;
+        v.lkv = it.lkv;
+        v.t = it.t;
+        v.unit = it.unit;
+        v.n_tiles = (hi + BN - 1) / BN;
+        v.q0 = min(it.q_start + it.t * h.tile_tokens, total_q - 2 * m_tok);
+        v.last = 0;
+        if (!(ok = publish(v))) break;
+        if (v.n_tiles == 0) continue;
+        const int g = v.unit;
         if (!(ok = mbar_wait(&bars->q_empty, (items & 1) ^ 1, abort, status))) break;
         mbar_arrive_expect_tx(&bars->q_full, q_bytes);
 #pragma unroll
@@ -153,10 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < C::KCH; ++c)
             tma_load_3d(smem + C::OFF_Q + t * C::Q_TILE + c * C::Q_CHUNK, &tmap_q, &bars->q_full,
-                        c * 64, g * G, pg.q0 + t * m_tok);
+                        c * 64, g * G, v.q0 + t * m_tok);
         ++items;
-        for (int j = 0; ok && j < pg.n_tiles; ++j) {
-          const int k0 = min(pg.it.kv_start + j * BN, total_kv - BN);
+        for (int j = 0; ok && j < v.n_tiles; ++j) {
+          const int k0 = min(v.kv_start + j * BN, total_kv - BN);
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv, ++loads) {
             const int sl = loads % C::SLOTS;
@@ -172,6 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (ok) {
+        ItemSlot v{};
+        v.last = 1;
+        publish(v);
+      }
       // Drain: every copy this thread issued must land before the CTA exits.
       if (items) mbar_wait(&bars->q_full, (items - 1) & 1, abort, status);
       for (int s = 0; s < C::SLOTS; ++s) {
@@ -186,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_o = idesc_f16<T>(kTcRows, D, false, true);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q);
       const uint32_t sRing = smem_u32(smem + C::OFF_RING);
-      uint32_t items = 0, loads = 0, tiles = 0;  // tiles: key tiles done (per query tile)
+      uint32_t items = 0, loads = 0, tiles = 0, taken = 0;
       bool ok = true;
       auto issue_s = [&](int t, uint32_t kslot) {
         const uint32_t q_a = sQ + t * C::Q_TILE;
@@ -215,9 +300,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         return r;
       };
-      for (int idx = blockIdx.x; ok && idx < h.n_items; idx += gridDim.x) {
-        const PairGeom pg = pair_geom(p, h, idx, total_q, m_tok);
-        const int n = pg.n_tiles;
+      while (ok) {
+        const int isl = taken % kItemSlots;
+        if (!(ok = mbar_wait(&bars->item_full[isl], (taken / kItemSlots) & 1, abort, status)))
+          break;
+        const int n = bars->items[isl].n_tiles, last = bars->items[isl].last;
+        mbar_arrive(&bars->item_empty[isl]);
+        ++taken;
+        if (last) break;
         if (n == 0) continue;
         if (!(ok = mbar_wait(&bars->q_full, items & 1, abort, status))) break;
         tc_fence_after();
@@ -269,22 +359,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t col_s = C::COL_S + tq * 128, col_o = C::COL_O + tq * D;
     const float NEG_INF = __int_as_float(0xff800000);
-    const bool capped = p.softcap != 0.0f;
-    const float s_mul = capped ? p.scale / p.softcap : p.scale * kLog2e;
+    const float s_mul = CAP ? p.scale / p.softcap : p.scale * kLog2e;
     const float cap_mul = p.softcap * kLog2e;
     const bool up = p.scale > 0.0f;  // direction of the (monotone) score transform
-    uint32_t tiles = 0;
+    const int span = 2 * m_tok;      // tokens per item
+    uint32_t tiles = 0, taken = 0;
     bool ok = true;
     T* out = static_cast<T*>(p.out);
 
-    for (int idx = blockIdx.x; ok && idx < h.n_items; idx += gridDim.x) {
-      const PairGeom pg = pair_geom(p, h, idx, total_q, m_tok);
-      const PrefillItem& it = pg.it;
-      const int n = pg.n_tiles;
-      const int tok = pg.q0 + tq * m_tok + r / G;
+    while (ok) {
+      const int isl = taken % kItemSlots;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->item_full[isl], (taken / kItemSlots) & 1,
+                                             abort, status));
+      if (!ok) break;
+      const ItemSlot it = bars->items[isl];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->item_empty[isl]);
+      ++taken;
+      if (it.last) break;
+      const int n = it.n_tiles;
+      const int tok = it.q0 + tq * m_tok + r / G;
       const int i = tok - it.q_start;
-      const int first = it.t * h.tile_tokens;
-      const bool own = r < G * m_tok && i >= first && i < min(first + h.tile_tokens, it.lq);
+      const int first = it.t * span;
+      const bool own = r < G * m_tok && i >= first && i < min(first + span, it.lq);
       const size_t orow = ((size_t)tok * p.H + (size_t)it.unit * G + (r % G)) * D;
       if (n == 0) {
         if (own) {
@@ -307,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int base = k0 - it.kv_start;  // local key index of column 0
         const int lo_c = j * BN - base;     // visible columns [lo_c, hi_c)
         const int hi_c = min((j + 1) * BN, row_hi) - base;
-        const bool full_tile = __all_sync(0xffffffffu, lo_c <= 0 && hi_c >= BN);
+        const bool masked = !__all_sync(0xffffffffu, lo_c <= 0 && hi_c >= BN);
         // Pass 1: extreme raw score over the visible columns.  The score
         // transform (scale, then optional softcap) is monotone -- increasing
         // for scale > 0, decreasing for scale < 0 -- so the row max of the
@@ -319,16 +416,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(t_lane + col_s + c, va);
           tmem_ld32(t_lane + col_s + c + 32, vb);
           tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            float x = __uint_as_float(e < 32 ? va[e] : vb[e - 32]);
-            if (!full_tile && (c + e < lo_c || c + e >= hi_c)) x = up ? NEG_INF : -NEG_INF;
-            ext = up ? fmaxf(ext, x) : fminf(ext, x);
+          if (up) {
+            ext = masked ? extreme64<true, true>(va, vb, c, lo_c, hi_c, ext)
+                         : extreme64<true, false>(va, vb, c, lo_c, hi_c, ext);
+          } else {
+            ext = masked ? extreme64<false, true>(va, vb, c, lo_c, hi_c, ext)
+                         : extreme64<false, false>(va, vb, c, lo_c, hi_c, ext);
           }
         }
         const float mt = (ext == NEG_INF || ext == -NEG_INF)
                              ? NEG_INF
-                             : (capped ? cap_mul * tanh_via_exp2(ext * s_mul) : ext * s_mul);
+                             : (CAP ? cap_mul * tanh_via_exp2(ext * s_mul) : ext * s_mul);
         const float m_new = fmaxf(m_used, mt);
         float alpha = 1.0f;
         if (m_new > m_used + kRescaleThreshold) {
@@ -354,9 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // Pass 2: p = 2^(x - m), row sum, P (16-bit pairs) into TMEM over the
-        // S columns already read: columns [c, c+32) of S become P columns
-        // [c/2, c/2 + 16).
-        float rs = 0.0f;
+        // S columns already read: columns [c, c+64) of S become P columns
+        // [c/2, c/2 + 32).
+        float2 rs = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int c = 0; c < BN; c += 64) {
           uint32_t va[32], vb[32];
@@ -364,32 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(t_lane + col_s + c + 32, vb);
           tmem_wait_ld();
           uint32_t pw[32];
-#pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            float pr[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int cc = e + u;
-              const float sraw = __uint_as_float(cc < 32 ? va[cc] : vb[cc - 32]);
-              float x = capped ? cap_mul * tanh_via_exp2(sraw * s_mul) - m_eff
-                               : fmaf(sraw, s_mul, -m_eff);
-              if (!full_tile && (c + cc < lo_c || c + cc >= hi_c)) x = NEG_INF;
-              pr[u] = ex2_approx(x);
-              rs += pr[u];
-            }
-            pw[e >> 1] = pack2<T>(pr[0], pr[1]);
-          }
-          uint32_t lo16[16], hi16[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            lo16[e] = pw[e];
-            hi16[e] = pw[16 + e];
-          }
-          tmem_st16(t_lane + col_s + (c >> 1), lo16);
-          tmem_st16(t_lane + col_s + (c >> 1) + 16, hi16);
+          if (masked)
+            exp64<T, CAP, true>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_eff, rs, pw);
+          else
+            exp64<T, CAP, false>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_eff, rs, pw);
+          tmem_st32(t_lane + col_s + (c >> 1), pw);
         }
         tmem_wait_st();
-        l = l * alpha + rs;
+        l = l * alpha + (rs.x + rs.y);
         tc_fence_before();
         mbar_arrive(&bars->p_full[tq]);
       }
@@ -430,14 +510,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc<C::TMEM_COLS>(tmem);
 }
 
-template <typename T, int D>
+template <typename T, int D, bool CAP>
 cudaError_t launch_pair(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, int num_sms, cudaStream_t s) {
   constexpr int smem = PairCfg<D>::SMEM;
-  auto kern = pva_prefill_pair_kernel<T, D>;
+  auto kern = pva_prefill_pair_kernel<T, D, CAP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return launch_dependent(kern, dim3(num_sms), dim3(kThreads), smem, s, p, tq, tk, tv);
+}
+
+template <typename T, int D>
+cudaError_t launch_pair_cap(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, int num_sms, cudaStream_t s) {
+  return p.softcap != 0.0f ? launch_pair<T, D, true>(p, tq, tk, tv, num_sms, s)
+                           : launch_pair<T, D, false>(p, tq, tk, tv, num_sms, s);
 }
 
 }  // namespace
@@ -448,11 +535,11 @@ cudaError_t launch_prefill_pair(const AttnParams& p, int dtype, const CUtensorMa
   const bool bf = dtype == PVA_BF16;
   switch (p.d) {
     case 64:
-      return bf ? launch_pair<__nv_bfloat16, 64>(p, tq, tk, tv, num_sms, s)
-                : launch_pair<__half, 64>(p, tq, tk, tv, num_sms, s);
+      return bf ? launch_pair_cap<__nv_bfloat16, 64>(p, tq, tk, tv, num_sms, s)
+                : launch_pair_cap<__half, 64>(p, tq, tk, tv, num_sms, s);
     case 128:
-      return bf ? launch_pair<__nv_bfloat16, 128>(p, tq, tk, tv, num_sms, s)
-                : launch_pair<__half, 128>(p, tq, tk, tv, num_sms, s);
+      return bf ? launch_pair_cap<__nv_bfloat16, 128>(p, tq, tk, tv, num_sms, s)
+                : launch_pair_cap<__half, 128>(p, tq, tk, tv, num_sms, s);
     default:
       return cudaErrorInvalidValue;
   }
