@@ -93,6 +93,8 @@ template <bool UP, bool MASKED>
 __device__ __forceinline__ float extreme64(const uint32_t (&va)[32], const uint32_t (&vb)[32],
                                            int c, int lo_c, int hi_c, float ext) {
   const float neutral = UP ? __int_as_float(0xff800000) : __int_as_float(0x7f800000);
+  // four independent partial extremes: no 32-long dependency chain
+  float acc[4] = {ext, neutral, neutral, neutral};
 #pragma unroll
   for (int e = 0; e < 64; e += 2) {
     float x0 = col_val(va, vb, e), x1 = col_val(va, vb, e + 1);
@@ -100,9 +102,11 @@ __device__ __forceinline__ float extreme64(const uint32_t (&va)[32], const uint3
       x0 = (c + e >= lo_c && c + e < hi_c) ? x0 : neutral;
       x1 = (c + e + 1 >= lo_c && c + e + 1 < hi_c) ? x1 : neutral;
     }
-    ext = UP ? fmax3f(ext, x0, x1) : fmin3f(ext, x0, x1);
+    float& a = acc[(e >> 1) & 3];
+    a = UP ? fmax3f(a, x0, x1) : fmin3f(a, x0, x1);
   }
-  return ext;
+  return UP ? fmaxf(fmax3f(acc[0], acc[1], acc[2]), acc[3])
+            : fminf(fmin3f(acc[0], acc[1], acc[2]), acc[3]);
 }
 
 // p = 2^(x - m) for columns [c, c+64), x the transformed score; row sums in
@@ -112,6 +116,7 @@ __device__ __forceinline__ void exp64(const uint32_t (&va)[32], const uint32_t (
                                       int lo_c, int hi_c, float s_mul, float cap_mul, float m_eff,
                                       float2& rs, uint32_t (&pw)[32]) {
   const float2 mul2 = make_float2(s_mul, s_mul), neg_m = make_float2(-m_eff, -m_eff);
+  float2 acc[2] = {rs, make_float2(0.0f, 0.0f)};  // two independent partial sums
 #pragma unroll
   for (int e = 0; e < 64; e += 2) {
     const float2 s = make_float2(col_val(va, vb, e), col_val(va, vb, e + 1));
@@ -128,9 +133,10 @@ __device__ __forceinline__ void exp64(const uint32_t (&va)[32], const uint32_t (
       x.y = (c + e + 1 >= lo_c && c + e + 1 < hi_c) ? x.y : ninf;
     }
     const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-    rs = fadd2(rs, p);
+    acc[(e >> 1) & 1] = fadd2(acc[(e >> 1) & 1], p);
     pw[e >> 1] = pack2<T>(p.x, p.y);
   }
+  rs = fadd2(acc[0], acc[1]);
 }
 
 template <typename T, int D, bool CAP>
