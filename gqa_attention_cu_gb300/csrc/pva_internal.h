@@ -35,7 +35,8 @@ __host__ __device__ constexpr int decode_tile_keys(int D) { return 8192 / D; }
 // ---- workspace layout (int32 words) ----------------------------------------
 // [0..8)         SchedHeader of the latest call
 // [8..)          prefill order [B], prefill prefix [B+1], decode order [B],
-//                decode prefix [B+1], decode completion counters [B*Hkv]
+//                decode prefix [B+1], decode completion counters [B*Hkv],
+//                work counters [4]
 // then (256-byte aligned) fp32 split partials [cap_units][G*dv + 2G].
 // The sticky status word lives in its own allocation (it never moves when
 // the workspace grows).
@@ -60,8 +61,10 @@ struct WsLayout {
   __host__ __device__ int dec_order() const { return kWsArrays + 2 * B + 1; }
   __host__ __device__ int dec_prefix() const { return kWsArrays + 3 * B + 1; }
   __host__ __device__ int dec_done() const { return kWsArrays + 4 * B + 2; }
+  // work counters the persistent kernels draw item indices from: [0] prefill, [1] decode
+  __host__ __device__ size_t counters() const { return (size_t)dec_done() + (size_t)B * Hkv; }
   __host__ __device__ size_t int_words() const {
-    size_t w = (size_t)kWsArrays + 4 * (size_t)B + 2 + (size_t)B * Hkv;
+    size_t w = counters() + 4;
     return (w + 63) / 64 * 64;
   }
 };

@@ -216,7 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++published;
         return true;
       };
-      for (int idx = blockIdx.x; ok && idx < h.n_items; idx += gridDim.x) {
+      // Items are drawn from a device-wide counter (zeroed by the scheduler):
+      // a CTA takes the next item of the longest-first list when it is ready
+      // for one, which balances uneven item costs across the persistent grid.
+      int* next_item = p.ws + WsLayout{p.B, p.Hkv}.counters();
+      for (int idx = atomicAdd(next_item, 1); ok && idx < h.n_items; idx = atomicAdd(next_item, 1)) {
         const PrefillItem it = decode_prefill_item(p, h, idx);
         const int hi = item_key_extent(it, h.tile_tokens, p.is_causal);
         ItemSlot v;

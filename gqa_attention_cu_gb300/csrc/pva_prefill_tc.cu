@@ -1,37 +1,35 @@
 // bf16/f16 prefill on the 5th-generation tensor cores (tcgen05 + TMEM) with
-// TMA-staged operands, for head sizes d = dv in {64, 128, 256}.
+// TMA-staged operands for head size d = dv = 256 (one 128-row query tile per
+// CTA: the 256-column O accumulator leaves TMEM room for one tile only).
 //
 // The arithmetic is the page's (packed_varlen_attention.rs, stages 1-5:
 // scale * q.k, optional softcap * tanh(score / softcap) before the mask, the
 // tail-aligned causal frontier j <= i + L_kv - L_q, max-subtracted
 // exponentials, zero rows when nothing is visible, weighted sum of V) but it
-// streams over key tiles with a running maximum (online softmax), so no score
-// matrix is ever stored.
+// streams over key tiles of 64 keys with a running maximum (online softmax),
+// so no score matrix is ever stored.
 //
-// Work item = (sequence, query tile, kv head g).  The G = H/Hkv query heads
-// that share kv head g are packed along the MMA's M dimension: a query tile
-// holds m = floor(128 / G) tokens x G heads = up to 128 rows, so every K/V
-// tile that is loaded serves all G heads (GQA reuse inside the CTA).
+// Work item = (sequence, query tile of m = floor(128/G) tokens x G heads, kv
+// head g): every K/V tile loaded serves all G query heads sharing it.
 //
 // Per CTA (persistent, one per SM, 192 threads):
-//   warp 0      TMA producer: Q tile once per item, then K/V tiles into a
-//               STAGES-deep ring (mbarrier full/empty pairs).
-//   warp 1      MMA issuer (one thread) + TMEM owner: S = Q K^T into one of
-//               two TMEM score buffers, O += P V into the TMEM accumulator.
-//   warps 2..5  softmax / correction / epilogue: one thread per TMEM lane
-//               (= MMA row).  Reads S with tcgen05.ld, applies scale,
-//               softcap and masks, keeps the running max and sum, writes P
-//               (16-bit) into shared memory in the 128-byte-swizzled layout
-//               the MMA reads, rescales O in TMEM when the max grows by more
-//               than 2^8 (lazily), and finally normalises O and stores the
-//               rows that belong to the item.
+//   warp 0      TMA producer: draws work items from a device-wide counter,
+//               publishes each decoded item through a shared-memory ring, and
+//               loads the Q tile, then K_j and V_j into a 5-slot ring.
+//   warp 1      MMA issuer + TMEM owner.  S is double-buffered in TMEM
+//               (S(j) in buffer j & 1), so S(j+1) runs while tile j is being
+//               exponentiated; P(j) (16-bit pairs) overwrites S(j)'s buffer and
+//               feeds O += P V with A taken from TMEM; S(j+2) reuses the buffer
+//               after that MMA (tcgen05 MMAs of one thread run in issue order).
+//   warps 2..5  softmax / correction / epilogue, one thread per TMEM lane.
+// TMEM: S buffers [0,64) and [64,128), O [128,384).  Shared memory: Q 64 KB +
+// 5 K/V slots of 32 KB.
 //
-// Key tiles beyond the causal frontier of an item's last row are never
-// loaded; the diagonal tile and the ragged last tile are masked per element.
-// Tiles that would run past the end of the packed buffers are shifted back
-// so they end at the buffer's last row (columns/rows that belong to other
-// positions are masked or discarded); tiles starting before row 0 are
-// zero-filled by the TMA unit.  Nothing outside [0, cu[B]) rows is read.
+// Softcap: tanh(t) of the scaled score t = s * scale / softcap comes from its
+// Maclaurin series t - t^3/3 + 2t^5/15 - 17t^7/315 + 62t^9/2835 -
+// 1382t^11/155925 (error < 4e-7 for |t| <= 1/2) on the FMA pipe whenever every
+// score of the warp's tile has |t| <= 1/2; otherwise from the identity
+// tanh(t) = 1 - 2 / (exp(2t) + 1).
 #include "pva_device.cuh"
 #include "pva_items.cuh"
 
@@ -41,56 +39,116 @@ namespace {
 constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows > 2^8
+constexpr int kItemSlots = 4;
+constexpr int kSoftmaxWarps = 4;
+constexpr float kPolyLimit = 0.5f;          // |t| range of the tanh series
 
 template <int D>
 struct TcCfg {
-  static constexpr int BN = tc_block_n(D);
-  static constexpr int STAGES = D == 64 ? 3 : 2;
+  static constexpr int BN = 64;
   static constexpr int KCH = D / 64;              // 128-byte column chunks of a row
   static constexpr int Q_CHUNK = kTcRows * 128;   // bytes of one chunk of the Q tile
   static constexpr int Q_BYTES = KCH * Q_CHUNK;
   static constexpr int KV_CHUNK = BN * 128;       // bytes of one chunk of a K or V tile
-  static constexpr int K_BYTES = KCH * KV_CHUNK;
-  static constexpr int STAGE_BYTES = 2 * K_BYTES;  // K then V
-  static constexpr int P_CHUNK = kTcRows * 128;   // 64 keys x 128 rows
-  static constexpr int P_BYTES = (BN / 64) * P_CHUNK;
+  static constexpr int KV_TILE = KCH * KV_CHUNK;
+  static constexpr int SLOTS = 5;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = Q_BYTES;
-  static constexpr int OFF_P = OFF_KV + STAGES * STAGE_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
-  static constexpr int N_BARS = 16;
-  static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 1024;  // + alignment slack
+  static constexpr int OFF_RING = Q_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + SLOTS * KV_TILE;
+  static constexpr int SMEM = OFF_BAR + 1024 + 1024;  // barriers/items + alignment slack
   static constexpr int TMEM_COLS = 512;
-  static constexpr int COL_S0 = 0, COL_S1 = BN, COL_O = 2 * BN;
+  static constexpr int COL_S = 0;                 // + BN * buffer
+  static constexpr int COL_O = 2 * BN;
   static_assert(2 * BN + D <= TMEM_COLS, "TMEM budget");
-  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(SMEM <= 232448 - 64, "shared memory budget");
+};
+
+struct ItemSlot {
+  int q_start, kv_start, lq, lkv;
+  int t, unit, n_tiles, q0;
+  int last;
+  int pad[3];
 };
 
 struct Bars {
-  uint64_t q_full, q_empty, p_full, o_ready, o_free, drain;
-  uint64_t s_full[2];
-  uint64_t kv_full[4], kv_empty[4];
+  uint64_t q_full, q_empty, o_ready, o_free, drain, pad;
+  uint64_t s_full[2], p_full[2];
+  uint64_t ring_full[8], ring_empty[8];
+  uint64_t item_full[kItemSlots], item_empty[kItemSlots];
+  ItemSlot items[kItemSlots];
 };
+static_assert(sizeof(Bars) <= 1024, "barrier block");
 
-struct ItemGeom {
-  PrefillItem it;
-  int n_tiles;   // key tiles to visit (0: every row fully masked)
-  int tile_q0;   // first packed token of the loaded Q tile (may be < q_start)
-};
-
-template <int D>
-__device__ __forceinline__ ItemGeom item_geom(const AttnParams& p, const SchedHeader& h, int idx,
-                                              int total_q) {
-  ItemGeom g;
-  g.it = decode_prefill_item(p, h, idx);
-  const int hi = item_key_extent(g.it, h.tile_tokens, p.is_causal);
-  g.n_tiles = (hi + TcCfg<D>::BN - 1) / TcCfg<D>::BN;
-  const int want = g.it.q_start + g.it.t * h.tile_tokens;
-  g.tile_q0 = min(want, total_q - h.tile_tokens);
-  return g;
+__device__ __forceinline__ float col32(const uint32_t (&va)[32], const uint32_t (&vb)[32], int e) {
+  return __uint_as_float(e < 32 ? va[e] : vb[e - 32]);
 }
 
-template <typename T, int D>
+// Extreme raw scores (max, and min for the softcap range test) of a 64-column
+// tile; MASKED skips the columns outside [lo_c, hi_c).
+template <bool MASKED>
+__device__ __forceinline__ void extremes64(const uint32_t (&va)[32], const uint32_t (&vb)[32],
+                                           int lo_c, int hi_c, float& mx, float& mn) {
+  const float ninf = __int_as_float(0xff800000), pinf = __int_as_float(0x7f800000);
+  float a[2] = {ninf, ninf}, b[2] = {pinf, pinf};
+#pragma unroll
+  for (int e = 0; e < 64; e += 2) {
+    const float x0 = col32(va, vb, e), x1 = col32(va, vb, e + 1);
+    const bool v0 = !MASKED || (e >= lo_c && e < hi_c);
+    const bool v1 = !MASKED || (e + 1 >= lo_c && e + 1 < hi_c);
+    a[(e >> 1) & 1] = fmax3f(a[(e >> 1) & 1], v0 ? x0 : ninf, v1 ? x1 : ninf);
+    b[(e >> 1) & 1] = fmin3f(b[(e >> 1) & 1], v0 ? x0 : pinf, v1 ? x1 : pinf);
+  }
+  mx = fmaxf(a[0], a[1]);
+  mn = fminf(b[0], b[1]);
+}
+
+// Maclaurin series of tanh through t^11 (|t| <= 1/2).
+__device__ __forceinline__ float tanh_series(float t) {
+  const float u = t * t;
+  float p = -0.008863235529902197f;
+  p = fmaf(p, u, 0.021869488536155203f);
+  p = fmaf(p, u, -0.05396825396825397f);
+  p = fmaf(p, u, 0.13333333333333333f);
+  p = fmaf(p, u, -0.3333333333333333f);
+  p = fmaf(p, u, 1.0f);
+  return t * p;
+}
+
+// 2^(x - m) over the 64 columns, row sum, P packed as 16-bit pairs.
+// MODE 0: no softcap; 1: softcap via the series; 2: softcap via exp/rcp.
+template <typename T, int MODE, bool MASKED>
+__device__ __forceinline__ float exp64(const uint32_t (&va)[32], const uint32_t (&vb)[32],
+                                       int lo_c, int hi_c, float s_mul, float cap_mul,
+                                       float m_eff, uint32_t (&pw)[32]) {
+  const float2 mul2 = make_float2(s_mul, s_mul), neg_m = make_float2(-m_eff, -m_eff);
+  float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+#pragma unroll
+  for (int e = 0; e < 64; e += 2) {
+    const float2 s = make_float2(col32(va, vb, e), col32(va, vb, e + 1));
+    float2 x;
+    if (MODE == 0) {
+      x = ffma2(s, mul2, neg_m);
+    } else if (MODE == 1) {
+      x.x = fmaf(cap_mul, tanh_series(s.x * s_mul), -m_eff);
+      x.y = fmaf(cap_mul, tanh_series(s.y * s_mul), -m_eff);
+    } else {
+      x.x = fmaf(cap_mul, tanh_via_exp2(s.x * s_mul), -m_eff);
+      x.y = fmaf(cap_mul, tanh_via_exp2(s.y * s_mul), -m_eff);
+    }
+    if (MASKED) {
+      const float ninf = __int_as_float(0xff800000);
+      x.x = (e >= lo_c && e < hi_c) ? x.x : ninf;
+      x.y = (e + 1 >= lo_c && e + 1 < hi_c) ? x.y : ninf;
+    }
+    const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    acc[(e >> 1) & 1] = fadd2(acc[(e >> 1) & 1], p);
+    pw[e >> 1] = pack2<T>(p.x, p.y);
+  }
+  const float2 r = fadd2(acc[0], acc[1]);
+  return r.x + r.y;
+}
+
+template <typename T, int D, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     pva_prefill_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap tmap_q,
                           const __grid_constant__ CUtensorMap tmap_k,
@@ -101,7 +159,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sQ = smem + C::OFF_Q;
-  uint8_t* sP = smem + C::OFF_P;
   Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
@@ -118,71 +175,110 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 0;
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
-    mbar_init(&bars->p_full, 128);
     mbar_init(&bars->o_ready, 1);
     mbar_init(&bars->o_free, 128);
     mbar_init(&bars->drain, 1);
-    mbar_init(&bars->s_full[0], 1);
-    mbar_init(&bars->s_full[1], 1);
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->p_full[b], 128);
+    }
+    for (int s = 0; s < C::SLOTS; ++s) {
+      mbar_init(&bars->ring_full[s], 1);
+      mbar_init(&bars->ring_empty[s], 1);
+    }
+    for (int s = 0; s < kItemSlots; ++s) {
+      mbar_init(&bars->item_full[s], 1);
+      mbar_init(&bars->item_empty[s], 1 + kSoftmaxWarps);
     }
     fence_mbar_init();
   }
   // Rows of the Q tile beyond G*m are never written by the TMA unit; start
-  // them (and everything else) from zeros so no stale bits reach the MMA.
+  // them from zeros so no stale bits reach the MMA.
   for (int i = threadIdx.x; i < C::Q_BYTES / 16; i += kThreads)
     reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 1) tmem_alloc<C::TMEM_COLS>(&s_tmem_base);
+  if (warp == 0 && lane == 0) {
+    prefetch_tensor_map(&tmap_q);
+    prefetch_tensor_map(&tmap_k);
+    prefetch_tensor_map(&tmap_v);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem_base;
   wait_prior_grid();  // the scheduler's work lists are complete from here on
   allow_next_grid();
-  const SchedHeader h = *reinterpret_cast<const SchedHeader*>(p.ws + kWsHeader);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tensor_map(&tmap_q);
-      prefetch_tensor_map(&tmap_k);
-      prefetch_tensor_map(&tmap_v);
-      uint32_t q_cnt = 0, kv_cnt = 0;
+      const SchedHeader h = *reinterpret_cast<const SchedHeader*>(p.ws + kWsHeader);
+      uint32_t q_cnt = 0, loads = 0, published = 0;
       const uint32_t q_bytes = (uint32_t)C::KCH * (uint32_t)(G * m_tok) * 128u;
       bool ok = true;
-      for (int idx = blockIdx.x; ok && idx < h.n_items; idx += gridDim.x) {
-        const ItemGeom ig = item_geom<D>(p, h, idx, total_q);
-        if (ig.n_tiles == 0) continue;
-        const int g = ig.it.unit;
+      auto publish = [&](const ItemSlot& v) -> bool {
+        const int sl = published % kItemSlots;
+        if (!mbar_wait(&bars->item_empty[sl], ((published / kItemSlots) & 1) ^ 1, abort, status))
+          return false;
+        bars->items[sl] = v;
+        mbar_arrive(&bars->item_full[sl]);
+        ++published;
+        return true;
+      };
+      // Items are drawn from a device-wide counter (zeroed by the scheduler):
+      // a CTA takes the next item of the longest-first list when it is ready
+      // for one, which balances uneven item costs across the persistent grid.
+      int* next_item = p.ws + WsLayout{p.B, p.Hkv}.counters();
+      for (int idx = atomicAdd(next_item, 1); ok && idx < h.n_items; idx = atomicAdd(next_item, 1)) {
+        const PrefillItem it = decode_prefill_item(p, h, idx);
+        const int hi = item_key_extent(it, h.tile_tokens, p.is_causal);
+        ItemSlot v;
+        v.q_start = it.q_start;
+        v.kv_start = it.kv_start;
+        v.lq = it.lq;
+        v.lkv = it.lkv;
+        v.t = it.t;
+        v.unit = it.unit;
+        v.n_tiles = (hi + BN - 1) / BN;
+        v.q0 = min(it.q_start + it.t * h.tile_tokens, total_q - m_tok);
+        v.last = 0;
+        if (!(ok = publish(v))) break;
+        if (v.n_tiles == 0) continue;
+        const int g = v.unit;
         if (!(ok = mbar_wait(&bars->q_empty, (q_cnt & 1) ^ 1, abort, status))) break;
         mbar_arrive_expect_tx(&bars->q_full, q_bytes);
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(sQ + c * C::Q_CHUNK, &tmap_q, &bars->q_full, c * 64, g * G, ig.tile_q0);
+          tma_load_3d(sQ + c * C::Q_CHUNK, &tmap_q, &bars->q_full, c * 64, g * G, v.q0);
         ++q_cnt;
-        for (int j = 0; j < ig.n_tiles; ++j, ++kv_cnt) {
-          const int st = kv_cnt % C::STAGES;
-          const uint32_t use = kv_cnt / C::STAGES;
-          if (!(ok = mbar_wait(&bars->kv_empty[st], (use & 1) ^ 1, abort, status))) break;
-          uint8_t* sK = smem + C::OFF_KV + st * C::STAGE_BYTES;
-          uint8_t* sV = sK + C::K_BYTES;
-          const int k0 = min(ig.it.kv_start + j * BN, total_kv - BN);
-          mbar_arrive_expect_tx(&bars->kv_full[st], (uint32_t)C::STAGE_BYTES);
+        for (int j = 0; ok && j < v.n_tiles; ++j) {
+          const int k0 = min(v.kv_start + j * BN, total_kv - BN);
 #pragma unroll
-          for (int c = 0; c < C::KCH; ++c) {
-            tma_load_3d(sK + c * C::KV_CHUNK, &tmap_k, &bars->kv_full[st], c * 64, g, k0);
-            tma_load_3d(sV + c * C::KV_CHUNK, &tmap_v, &bars->kv_full[st], c * 64, g, k0);
+          for (int kv = 0; kv < 2; ++kv, ++loads) {
+            const int sl = loads % C::SLOTS;
+            if (!(ok = mbar_wait(&bars->ring_empty[sl], ((loads / C::SLOTS) & 1) ^ 1, abort,
+                                 status)))
+              break;
+            uint8_t* dst = smem + C::OFF_RING + sl * C::KV_TILE;
+            mbar_arrive_expect_tx(&bars->ring_full[sl], (uint32_t)C::KV_TILE);
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c)
+              tma_load_3d(dst + c * C::KV_CHUNK, kv ? &tmap_v : &tmap_k, &bars->ring_full[sl],
+                          c * 64, g, k0);
           }
         }
       }
+      if (ok) {
+        ItemSlot v{};
+        v.last = 1;
+        publish(v);
+      }
       // Drain: every copy this thread issued must land before the CTA exits.
       if (q_cnt) mbar_wait(&bars->q_full, (q_cnt - 1) & 1, abort, status);
-      for (int s = 0; s < C::STAGES; ++s) {
-        const uint32_t fills = kv_cnt > (uint32_t)s ? (kv_cnt - 1 - s) / C::STAGES + 1 : 0;
-        if (fills) mbar_wait(&bars->kv_full[s], (fills - 1) & 1, abort, status);
+      for (int s = 0; s < C::SLOTS; ++s) {
+        const uint32_t fills = loads > (uint32_t)s ? (loads - 1 - s) / C::SLOTS + 1 : 0;
+        if (fills) mbar_wait(&bars->ring_full[s], (fills - 1) & 1, abort, status);
       }
     }
   } else if (warp == 1) {
@@ -190,52 +286,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_f16<T>(kTcRows, BN, false, false);
       constexpr uint32_t idesc_o = idesc_f16<T>(kTcRows, D, false, true);
-      const uint32_t sQ_a = smem_u32(sQ), sP_a = smem_u32(sP);
-      uint32_t q_cnt = 0, gt = 0, items = 0;
+      const uint32_t sQ_a = smem_u32(sQ), sRing = smem_u32(smem + C::OFF_RING);
+      uint32_t q_cnt = 0, loads = 0, gt = 0, items = 0, taken = 0;
       bool ok = true;
-      for (int idx = blockIdx.x; ok && idx < h.n_items; idx += gridDim.x) {
-        const ItemGeom ig = item_geom<D>(p, h, idx, total_q);
-        const int n = ig.n_tiles;
+      auto wait_slot = [&](uint32_t L) -> bool {
+        const bool r = mbar_wait(&bars->ring_full[L % C::SLOTS], (L / C::SLOTS) & 1, abort, status);
+        tc_fence_after();
+        return r;
+      };
+      // S for global key tile T_ into buffer T_ & 1 from the K in load slot L
+      auto issue_s = [&](uint32_t T_, uint32_t L) {
+        const uint32_t k_a = sRing + (L % C::SLOTS) * C::KV_TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          mma_ss(tmem + C::COL_S + (T_ & 1) * BN,
+                 sdesc_sw128(sQ_a + (kk >> 2) * C::Q_CHUNK + off, 16, 1024),
+                 sdesc_sw128(k_a + (kk >> 2) * C::KV_CHUNK + off, 16, 1024), idesc_s,
+                 kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->s_full[T_ & 1]);
+        mma_commit(&bars->ring_empty[L % C::SLOTS]);  // K no longer needed once done
+      };
+      while (ok) {
+        const int isl = taken % kItemSlots;
+        if (!(ok = mbar_wait(&bars->item_full[isl], (taken / kItemSlots) & 1, abort, status)))
+          break;
+        const int n = bars->items[isl].n_tiles, last = bars->items[isl].last;
+        mbar_arrive(&bars->item_empty[isl]);
+        ++taken;
+        if (last) break;
         if (n == 0) continue;
         if (!(ok = mbar_wait(&bars->q_full, q_cnt & 1, abort, status))) break;
         tc_fence_after();
-        for (int j = 0; ok && j <= n; ++j) {
-          if (j < n) {
-            const uint32_t T_ = gt + j;
-            const int st = T_ % C::STAGES;
-            if (!(ok = mbar_wait(&bars->kv_full[st], (T_ / C::STAGES) & 1, abort, status))) break;
-            tc_fence_after();
-            const uint32_t sK_a = smem_u32(smem + C::OFF_KV + st * C::STAGE_BYTES);
-            const uint32_t d_s = tmem + ((T_ & 1) ? C::COL_S1 : C::COL_S0);
+        // key tile j: K in load slot loads + 2j, V in loads + 2j + 1
+        for (int j = 0; ok && j < 2 && j < n; ++j) {
+          if (!(ok = wait_slot(loads + 2 * j))) break;
+          issue_s(gt + j, loads + 2 * j);
+        }
+        if (!ok) break;
+        if (n <= 2) mma_commit(&bars->q_empty);
+        for (int j = 0; ok && j < n; ++j) {
+          const uint32_t T_ = gt + j, Lv = loads + 2 * j + 1;
+          if (j == 0 && !(ok = mbar_wait(&bars->o_free, (items & 1) ^ 1, abort, status))) break;
+          if (!(ok = mbar_wait(&bars->p_full[T_ & 1], (T_ >> 1) & 1, abort, status))) break;
+          if (!(ok = wait_slot(Lv))) break;
+          const uint32_t v_a = sRing + (Lv % C::SLOTS) * C::KV_TILE;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t koff = (kk & 3) * 32;
-              const uint64_t a = sdesc_sw128(sQ_a + (kk >> 2) * C::Q_CHUNK + koff, 16, 1024);
-              const uint64_t b = sdesc_sw128(sK_a + (kk >> 2) * C::KV_CHUNK + koff, 16, 1024);
-              mma_ss(d_s, a, b, idesc_s, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&bars->s_full[T_ & 1]);
-            if (j == n - 1) mma_commit(&bars->q_empty);
-          }
-          if (j > 0) {
-            const uint32_t T_ = gt + j - 1;
-            const int st = T_ % C::STAGES;
-            if (j == 1 && !(ok = mbar_wait(&bars->o_free, (items & 1) ^ 1, abort, status))) break;
-            if (!(ok = mbar_wait(&bars->p_full, T_ & 1, abort, status))) break;
-            tc_fence_after();
-            const uint32_t sV_a =
-                smem_u32(smem + C::OFF_KV + st * C::STAGE_BYTES + C::K_BYTES);
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              const uint64_t a =
-                  sdesc_sw128(sP_a + (kk >> 2) * C::P_CHUNK + (kk & 3) * 32, 16, 1024);
-              const uint64_t b = sdesc_sw128(sV_a + kk * 16 * 128, C::KV_CHUNK, 1024);
-              mma_ss(tmem + C::COL_O, a, b, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(&bars->kv_empty[st]);
-            mma_commit(&bars->o_ready);
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tmem + C::COL_O, tmem + C::COL_S + (T_ & 1) * BN + kk * 8,
+                   sdesc_sw128(v_a + kk * 16 * 128, C::KV_CHUNK, 1024), idesc_o,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars->o_ready);
+          mma_commit(&bars->ring_empty[Lv % C::SLOTS]);
+          if (j + 2 < n) {
+            if (!(ok = wait_slot(loads + 2 * (j + 2)))) break;
+            issue_s(T_ + 2, loads + 2 * (j + 2));
+            if (j + 3 == n) mma_commit(&bars->q_empty);
           }
         }
+        loads += 2 * n;
         gt += n;
         ++q_cnt;
         ++items;
@@ -250,20 +360,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
     const float NEG_INF = __int_as_float(0xff800000);
-    const bool capped = p.softcap != 0.0f;
-    const float s_mul = capped ? p.scale / p.softcap : p.scale * kLog2e;
+    const float s_mul = CAP ? p.scale / p.softcap : p.scale * kLog2e;
     const float cap_mul = p.softcap * kLog2e;
-    uint32_t gt = 0, items = 0;
+    const bool up = p.scale > 0.0f;  // direction of the (monotone) score transform
+    uint32_t gt = 0, taken = 0;
     bool ok = true;
     T* out = static_cast<T*>(p.out);
 
-    for (int idx = blockIdx.x; ok && idx < h.n_items; idx += gridDim.x) {
-      const ItemGeom ig = item_geom<D>(p, h, idx, total_q);
-      const PrefillItem& it = ig.it;
-      const int n = ig.n_tiles;
-      const int tok = ig.tile_q0 + r / G;  // packed token of this row
-      const int i = tok - it.q_start;       // its local query position
-      const bool own = r < G * m_tok && i >= it.t * m_tok && i < min((it.t + 1) * m_tok, it.lq);
+    while (ok) {
+      const int isl = taken % kItemSlots;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->item_full[isl], (taken / kItemSlots) & 1,
+                                             abort, status));
+      if (!ok) break;
+      const ItemSlot it = bars->items[isl];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->item_empty[isl]);
+      ++taken;
+      if (it.last) break;
+      const int n = it.n_tiles;
+      const int tok = it.q0 + r / G;  // packed token of this row
+      const int i = tok - it.q_start;  // its local query position
+      const int first = it.t * m_tok;
+      const bool own = r < G * m_tok && i >= first && i < min(first + m_tok, it.lq);
       const size_t orow = ((size_t)tok * p.H + (size_t)it.unit * G + (r % G)) * D;
       if (n == 0) {
         if (own) {
@@ -279,34 +397,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       for (int j = 0; j < n; ++j) {
         const uint32_t T_ = gt + j;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[T_ & 1], (T_ >> 1) & 1, abort, status));
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&bars->s_full[T_ & 1], (T_ >> 1) & 1, abort, status));
         if (!ok) break;
         tc_fence_after();
-        float s[BN];
-        {
-          const uint32_t col = (T_ & 1) ? C::COL_S1 : C::COL_S0;
-#pragma unroll
-          for (int c = 0; c < BN; c += 32) {
-            uint32_t v[32];
-            tmem_ld32(t_lane + col + c, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) s[c + e] = __uint_as_float(v[e]);
-          }
-        }
-        // visible columns [lo_c, hi_c) of this key tile
+        const uint32_t col_s = C::COL_S + (T_ & 1) * BN;
+        uint32_t va[32], vb[32];
+        tmem_ld32(t_lane + col_s, va);
+        tmem_ld32(t_lane + col_s + 32, vb);
+        tmem_wait_ld();
         const int k0 = min(it.kv_start + j * BN, total_kv - BN);
         const int base = k0 - it.kv_start;  // local key index of column 0
-        const int lo_c = j * BN - base;
+        const int lo_c = j * BN - base;     // visible columns [lo_c, hi_c)
         const int hi_c = min((j + 1) * BN, row_hi) - base;
+        const bool masked = !__all_sync(0xffffffffu, lo_c <= 0 && hi_c >= BN);
+        float mx, mn;
+        if (masked)
+          extremes64<true>(va, vb, lo_c, hi_c, mx, mn);
+        else
+          extremes64<false>(va, vb, lo_c, hi_c, mx, mn);
+        const float ext = up ? mx : mn;  // the transform is monotone in the raw score
+        const bool any = mx != NEG_INF;
         float mt = NEG_INF;
-#pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          float x = capped ? cap_mul * tanh_via_exp2(s[c] * s_mul) : s[c] * s_mul;
-          x = (c >= lo_c && c < hi_c) ? x : NEG_INF;
-          s[c] = x;
-          mt = fmaxf(mt, x);
-        }
+        if (any) mt = CAP ? cap_mul * tanh_via_exp2(ext * s_mul) : ext * s_mul;
         const float m_new = fmaxf(m_used, mt);
         float alpha = 1.0f;
         if (m_new > m_used + kRescaleThreshold) {
@@ -314,17 +427,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_used = m_new;
         }
         const float m_eff = m_used == NEG_INF ? 0.0f : m_used;
-        float rs = 0.0f;
-#pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          s[c] = ex2_approx(s[c] - m_eff);
-          rs += s[c];
+        uint32_t pw[32];
+        float rs;
+        if (!CAP) {
+          rs = masked ? exp64<T, 0, true>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw)
+                      : exp64<T, 0, false>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw);
+        } else {
+          // every visible score of the warp has |t| <= 1/2: tanh from its series
+          const float tmax = fmaxf(fabsf(mx * s_mul), fabsf(mn * s_mul));
+          const bool series = __all_sync(0xffffffffu, !any || tmax <= kPolyLimit);
+          if (series)
+            rs = masked ? exp64<T, 1, true>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw)
+                        : exp64<T, 1, false>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw);
+          else
+            rs = masked ? exp64<T, 2, true>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw)
+                        : exp64<T, 2, false>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw);
         }
+        // P (16-bit pairs) over the S buffer's first 32 columns
+        tmem_st32(t_lane + col_s, pw);
         l = l * alpha + rs;
-
         if (j > 0) {
-          // PV of the previous tile must be complete: it reads the P buffer
-          // we are about to overwrite and accumulates into O.
+          // O must hold PV(j-1) before it is rescaled (and before PV(j)).
           ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready, (T_ - 1) & 1, abort, status));
           if (!ok) break;
           tc_fence_after();
@@ -338,25 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
               tmem_st32(t_lane + C::COL_O + c, v);
             }
-            tmem_wait_st();
           }
         }
-        // P (16-bit) -> shared memory, K-major, 128-byte swizzle: row r,
-        // 16-byte chunk q of a 64-key half lands at chunk q ^ (r & 7).
-#pragma unroll
-        for (int c = 0; c < BN; c += 8) {
-          uint4 w;
-          w.x = pack2<T>(s[c + 0], s[c + 1]);
-          w.y = pack2<T>(s[c + 2], s[c + 3]);
-          w.z = pack2<T>(s[c + 4], s[c + 5]);
-          w.w = pack2<T>(s[c + 6], s[c + 7]);
-          const int half = c >> 6, q16 = (c & 63) >> 3;
-          uint8_t* dst = sP + half * C::P_CHUNK + r * 128 + ((q16 ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) = w;
-        }
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->p_full);
+        mbar_arrive(&bars->p_full[T_ & 1]);
       }
       if (!ok) break;
 
@@ -386,7 +495,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->o_free);
       gt += n;
-      ++items;
     }
   }
 
@@ -396,14 +504,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc<C::TMEM_COLS>(tmem);
 }
 
-template <typename T, int D>
+template <typename T, int D, bool CAP>
 cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                       const CUtensorMap& tv, int num_sms, cudaStream_t s) {
   constexpr int smem = TcCfg<D>::SMEM;
-  auto kern = pva_prefill_tc_kernel<T, D>;
+  auto kern = pva_prefill_tc_kernel<T, D, CAP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return launch_dependent(kern, dim3(num_sms), dim3(kThreads), smem, s, p, tq, tk, tv);
+}
+
+template <typename T>
+cudaError_t launch_tc_cap(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, int num_sms, cudaStream_t s) {
+  return p.softcap != 0.0f ? launch_tc<T, 256, true>(p, tq, tk, tv, num_sms, s)
+                           : launch_tc<T, 256, false>(p, tq, tk, tv, num_sms, s);
 }
 
 }  // namespace
@@ -411,14 +526,9 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tq, const CUtensor
 cudaError_t launch_prefill_tc(const AttnParams& p, int dtype, const CUtensorMap& tq,
                               const CUtensorMap& tk, const CUtensorMap& tv, int num_sms,
                               cudaStream_t s) {
-  const bool bf = dtype == PVA_BF16;
-  switch (p.d) {
-    case 256:
-      return bf ? launch_tc<__nv_bfloat16, 256>(p, tq, tk, tv, num_sms, s)
-                : launch_tc<__half, 256>(p, tq, tk, tv, num_sms, s);
-    default:
-      return cudaErrorInvalidValue;
-  }
+  if (p.d != 256) return cudaErrorInvalidValue;
+  return dtype == PVA_BF16 ? launch_tc_cap<__nv_bfloat16>(p, tq, tk, tv, num_sms, s)
+                           : launch_tc_cap<__half>(p, tq, tk, tv, num_sms, s);
 }
 
 }  // namespace pva

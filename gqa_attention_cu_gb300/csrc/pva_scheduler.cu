@@ -13,7 +13,8 @@
 //   * a decode list: sequences with L_q == 1 (when routing is on), longest
 //     first, each split into S_b key chunks, with a prefix of their
 //     (kv head, split) unit counts;
-//   * zeroed split-completion counters for the decode combine.
+//   * zeroed split-completion counters for the decode combine, and zeroed
+//     work counters from which the persistent compute kernels draw items.
 //
 // One CTA of 1024 threads.  B <= 2048 sequences are sorted in shared memory
 // (bitonic); larger batches keep their input order.
@@ -217,6 +218,7 @@ __global__ void __launch_bounds__(kThreads) pva_schedule_kernel(AttnParams p, Sc
   // Completion counters of the decode combine start at zero every call.
   int32_t* done = ws + L.dec_done();
   for (long long i = threadIdx.x; i < (long long)B * p.Hkv; i += kThreads) done[i] = 0;
+  if (threadIdx.x < 4) ws[L.counters() + threadIdx.x] = 0;  // work counters of this call
   __syncthreads();
 
   int n_pref = 0, n_items = 0, n_dec = 0, n_units = 0;
