@@ -10,8 +10,10 @@
 // Work unit = (sequence, kv head g, split s): the keys of a sequence are cut
 // into S_b splits (chosen on the device by the scheduler).  Per CTA
 // (persistent, one per SM):
-//   warp 0      TMA producer: K and V tiles of TK keys (16 KB each, rows of
-//               d contiguous elements) into a 4-stage ring.
+//   warp 0      TMA producer: draws units from a device-wide counter,
+//               publishes each decoded unit through a shared-memory ring, and
+//               streams its K and V tiles of TK keys (16 KB each, rows of d
+//               contiguous elements) into a 4-stage ring.
 //   warps 1..8  compute.  A round covers R = 32/G keys x G heads = 32
 //               (key, head) pairs: lane l owns d/32 consecutive dims of every
 //               key, forms the 32 partial dot products, and a reduce-scatter
@@ -33,6 +35,7 @@ constexpr int kComputeWarps = 8;
 constexpr int kThreads = 32 * (1 + kComputeWarps);
 constexpr int kStages = 4;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kUnitSlots = 4;
 
 template <int D, int G>
 struct DecCfg {
@@ -47,7 +50,8 @@ struct DecCfg {
   static constexpr int OFF_P = OFF_ML + 2 * kComputeWarps * G * 4;   // [8][32] p
   static constexpr int OFF_A = OFF_P + kComputeWarps * 32 * 4;       // [8][G] alpha
   static constexpr int OFF_BAR = OFF_A + kComputeWarps * G * 4;
-  static constexpr int SMEM = OFF_BAR + 2 * kStages * 8 + 128;
+  static constexpr int OFF_UNITS = OFF_BAR + 2 * kStages * 8 + 2 * kUnitSlots * 8;
+  static constexpr int SMEM = OFF_UNITS + kUnitSlots * 64 + 128;
   static_assert(RPT >= 1, "tile shorter than a round");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -56,7 +60,10 @@ struct Unit {
   int b, g, s, S;      // sequence, kv head, split index, split count
   int ks, ke;          // key range [ks, ke) local to the sequence
   int kv_start, q_tok;
+  int u, last;         // unit index (partial slot); 1: no more units for this CTA
+  int pad[6];
 };
+static_assert(sizeof(Unit) == 64, "unit slot");
 
 __device__ __forceinline__ Unit decode_unit(const AttnParams& p, const SchedHeader& h, int u) {
   const WsLayout L{p.B, p.Hkv};
@@ -140,6 +147,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sA = reinterpret_cast<float*>(smem + C::OFF_A);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + kStages;
+  uint64_t* unit_full = empty + kStages;
+  uint64_t* unit_empty = unit_full + kUnitSlots;
+  Unit* units = reinterpret_cast<Unit*>(smem + C::OFF_UNITS);
   __shared__ int s_abort, s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -153,6 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kComputeWarps);
     }
+    for (int s = 0; s < kUnitSlots; ++s) {
+      mbar_init(&unit_full[s], 1);
+      mbar_init(&unit_empty[s], kComputeWarps);
+    }
     fence_mbar_init();
   }
   __syncthreads();
@@ -164,10 +178,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       prefetch_tensor_map(&tmap_k);
       prefetch_tensor_map(&tmap_v);
-      uint32_t cnt = 0;
+      uint32_t cnt = 0, published = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < h.n_units; u += gridDim.x) {
-        const Unit un = decode_unit(p, h, u);
+      auto publish = [&](const Unit& v) -> bool {
+        const int sl = published % kUnitSlots;
+        if (!mbar_wait(&unit_empty[sl], ((published / kUnitSlots) & 1) ^ 1, abort, status))
+          return false;
+        units[sl] = v;
+        mbar_arrive(&unit_full[sl]);
+        ++published;
+        return true;
+      };
+      // Units are drawn from a device-wide counter (zeroed by the scheduler),
+      // so CTAs that finish early take the next unit of the longest-first list.
+      int* next_unit = p.ws + WsLayout{p.B, p.Hkv}.counters() + 1;
+      for (int u = atomicAdd(next_unit, 1); ok && u < h.n_units; u = atomicAdd(next_unit, 1)) {
+        Unit un = decode_unit(p, h, u);
+        un.u = u;
+        un.last = 0;
+        if (!(ok = publish(un))) break;
         const int nt = (un.ke - un.ks + TK - 1) / TK;
         for (int j = 0; j < nt; ++j, ++cnt) {
           const int st = cnt % kStages;
@@ -178,6 +207,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(dk, &tmap_k, &full[st], 0, un.g, k0);
           tma_load_3d(dk + C::TILE_BYTES, &tmap_v, &full[st], 0, un.g, k0);
         }
+      }
+      if (ok) {
+        Unit v{};
+        v.last = 1;
+        publish(v);
       }
       for (int s = 0; s < kStages; ++s) {
         const uint32_t fills = cnt > (uint32_t)s ? (cnt - 1 - s) / kStages + 1 : 0;
@@ -196,8 +230,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t cnt = 0;
     bool ok = true;
 
-    for (int u = blockIdx.x; ok && u < h.n_units; u += gridDim.x) {
-      const Unit un = decode_unit(p, h, u);
+    uint32_t taken = 0;
+    while (ok) {
+      const int usl = taken % kUnitSlots;
+      ok = __all_sync(0xffffffffu, mbar_wait(&unit_full[usl], (taken / kUnitSlots) & 1, abort,
+                                             status));
+      if (!ok) break;
+      const Unit un = units[usl];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&unit_empty[usl]);
+      ++taken;
+      if (un.last) break;
+      const int u = un.u;
       const int nt = (un.ke - un.ks + TK - 1) / TK;
 
       float q[G][DPL];
@@ -238,10 +282,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             load_dims<T, DPL>(sK + (size_t)(r0 + r) * D * 2, lane, kf);
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
-              float a = 0.0f;
+              float2 a = make_float2(0.0f, 0.0f);
 #pragma unroll
-              for (int e = 0; e < DPL; ++e) a = fmaf(q[hh][e], kf[e], a);
-              v[r * G + hh] = a;
+              for (int e = 0; e < DPL; e += 2)
+                a = ffma2(make_float2(q[hh][e], q[hh][e + 1]), make_float2(kf[e], kf[e + 1]), a);
+              v[r * G + hh] = a.x + a.y;
             }
           }
           // reduce-scatter: after the 5 steps lane l holds the full dot of pair l
@@ -287,7 +332,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int hh = 0; hh < G; ++hh)
 #pragma unroll
-              for (int e = 0; e < DPL; ++e) acc[hh][e] = fmaf(pw[hh], vf[e], acc[hh][e]);
+              for (int e = 0; e < DPL; e += 2) {
+                const float2 a = ffma2(make_float2(pw[hh], pw[hh]), make_float2(vf[e], vf[e + 1]),
+                                       make_float2(acc[hh][e], acc[hh][e + 1]));
+                acc[hh][e] = a.x;
+                acc[hh][e + 1] = a.y;
+              }
           }
           __syncwarp();
         }
