@@ -306,6 +306,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-seconds", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="draw only this many sequences of the workload's recipe "
+                         "(smaller cases for profiler captures; not a bench line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -328,7 +331,7 @@ def main():
     pva.load_library()
 
     w_name = args.workload
-    w = workloads.make(w_name, seed=rank, device=str(dev))
+    w = workloads.make(w_name, seed=rank, device=str(dev), B=args.batch)
     H, Hkv, d, dv = w["num_heads"], w["kv_num_heads"], w["head_size"], w["v_head_size"]
     flops, kv_bytes = work_units(w)
     is_decode = w_name == "bf16_decode"
@@ -427,13 +430,15 @@ def main():
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks[key], "unit": "TFLOP/s",
                 "frac": achieved / peaks[key],
                 "traffic": recorded_traffic(f"prefill_{w_name}"),
-                "kernel": "pva_prefill_tc_kernel" if w["dtype"] != "f32" else "pva_prefill_f32_kernel",
+                "kernel": ("pva_prefill_f32_kernel" if w["dtype"] == "f32" else
+                           "pva_prefill_pair_kernel" if w["head_size"] <= 128 else "pva_prefill_tc_kernel"),
                 "peak_source": peaks["source"] + " " + key + " (burst: kernel timed alone)"}
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[w_name], "name": w_name,
+                   **({"batch_override": args.batch} if args.batch else {}),
                    "l2": "flushed between steps (256 MB write); inputs also exceed L2"
                    if not is_decode else "flushed between steps; K/V (4.6 GB) exceed L2",
                    "tokens_q": int(w["cu_q"][-1]), "tokens_kv": int(w["cu_kv"][-1]),

@@ -26,7 +26,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-__device__ __forceinline__ bool elect_one_lane() { return (threadIdx.x & 31) == 0; }
+// One lane of the (fully active) warp, chosen by elect.sync.  A role run by
+// the whole warp keeps its loop state warp-uniform, so the operands of the
+// tcgen05/TMA instructions that the chosen lane issues can stay in uniform
+// registers instead of being moved there before every instruction.
+__device__ __forceinline__ bool elect_sync() {
+  uint32_t is;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(is));
+  return is != 0;
+}
 
 // Programmatic dependent launch: wait until the preceding grid on the stream
 // has completed and its writes are visible (a no-op when the kernel was not
@@ -145,14 +155,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// try_wait with a suspend-time hint: while the phase is incomplete the
+// hardware may park the thread for up to `hint_ns` (it wakes when the phase
+// completes), so a waiting warp takes no issue slots from the warps sharing
+// its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -161,15 +176,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // up after PVA_WAIT_LIMIT_NS (or as soon as another role has given up, which
 // it signals through *abort): sets the abort flag and the device status bit
 // and returns false.  Every pipeline wait in this library goes through here.
+// Each attempt may sleep up to PVA_WAIT_SLICE_NS, so the limit is checked
+// with that granularity.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status,
                                           uint64_t limit_ns = PVA_WAIT_LIMIT_NS) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait_sleep(bar, parity, PVA_WAIT_SLICE_NS)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, PVA_WAIT_SLICE_NS)) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > limit_ns) {
       *abort = 1;
@@ -317,6 +332,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)2 << 61;
   return d;
+}
+
+// The same descriptor advanced by a byte offset: the start-address field holds
+// addr >> 4 in its low 14 bits, and shared-memory addresses stay below
+// 256 KB, so the offset adds without carrying into other fields.  Lets the
+// MMA issuer keep one base descriptor per buffer and add compile-time
+// constants instead of rebuilding descriptors in the issue loop.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t byte_offset) {
+  return desc + (uint64_t)(byte_offset >> 4);
 }
 
 // Instruction descriptor for kind::f16: fp32 accumulator (bits [4,6) = 1),

@@ -13,6 +13,7 @@
 #include "pva.h"
 
 #define PVA_WAIT_LIMIT_NS 2000000000ull  // 2 s: no legitimate pipeline wait comes close
+#define PVA_WAIT_SLICE_NS 100000u        // longest single sleep of a waiting thread (0.1 ms)
 
 namespace pva {
 

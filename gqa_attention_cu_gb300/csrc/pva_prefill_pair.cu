@@ -74,7 +74,7 @@ struct ItemSlot {
 
 struct PairBars {
   uint64_t q_full, q_empty, drain, pad;
-  uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];
+  uint64_t s_full[2], p_half[2], p_full[2], o_ready[2], o_free[2];
   uint64_t ring_full[kMaxSlots], ring_empty[kMaxSlots];
   uint64_t item_full[kItemSlots], item_empty[kItemSlots];
   ItemSlot items[kItemSlots];
@@ -110,36 +110,42 @@ __device__ __forceinline__ float extreme64(const uint32_t (&va)[32], const uint3
 }
 
 // p = 2^(x - m) for columns [c, c+64), x the transformed score; row sums in
-// rs; p packed as 16-bit pairs into pw.
+// rs; p packed as 16-bit pairs into pw.  Written as separate sweeps (all
+// exponents, then all ex2, then sums and packing) so that 64 independent
+// ex2 are in flight behind each other.
 template <typename T, bool CAP, bool MASKED>
 __device__ __forceinline__ void exp64(const uint32_t (&va)[32], const uint32_t (&vb)[32], int c,
                                       int lo_c, int hi_c, float s_mul, float cap_mul, float m_eff,
                                       float2& rs, uint32_t (&pw)[32]) {
   const float2 mul2 = make_float2(s_mul, s_mul), neg_m = make_float2(-m_eff, -m_eff);
-  float2 acc[2] = {rs, make_float2(0.0f, 0.0f)};  // two independent partial sums
+  float2 x[32];
 #pragma unroll
   for (int e = 0; e < 64; e += 2) {
-    const float2 s = make_float2(col_val(va, vb, e), col_val(va, vb, e + 1));
-    float2 x;
+    const float2 sc = make_float2(col_val(va, vb, e), col_val(va, vb, e + 1));
     if (CAP) {
-      x.x = cap_mul * tanh_via_exp2(s.x * s_mul) - m_eff;
-      x.y = cap_mul * tanh_via_exp2(s.y * s_mul) - m_eff;
+      x[e >> 1].x = cap_mul * tanh_via_exp2(sc.x * s_mul) - m_eff;
+      x[e >> 1].y = cap_mul * tanh_via_exp2(sc.y * s_mul) - m_eff;
     } else {
-      x = ffma2(s, mul2, neg_m);
+      x[e >> 1] = ffma2(sc, mul2, neg_m);
     }
     if (MASKED) {
       const float ninf = __int_as_float(0xff800000);
-      x.x = (c + e >= lo_c && c + e < hi_c) ? x.x : ninf;
-      x.y = (c + e + 1 >= lo_c && c + e + 1 < hi_c) ? x.y : ninf;
+      x[e >> 1].x = (c + e >= lo_c && c + e < hi_c) ? x[e >> 1].x : ninf;
+      x[e >> 1].y = (c + e + 1 >= lo_c && c + e + 1 < hi_c) ? x[e >> 1].y : ninf;
     }
-    const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-    acc[(e >> 1) & 1] = fadd2(acc[(e >> 1) & 1], p);
-    pw[e >> 1] = pack2<T>(p.x, p.y);
+  }
+#pragma unroll
+  for (int k = 0; k < 32; ++k) x[k] = make_float2(ex2_approx(x[k].x), ex2_approx(x[k].y));
+  float2 acc[2] = {rs, make_float2(0.0f, 0.0f)};  // two independent partial sums
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    acc[k & 1] = fadd2(acc[k & 1], x[k]);
+    pw[k] = pack2<T>(x[k].x, x[k].y);
   }
   rs = fadd2(acc[0], acc[1]);
 }
 
-template <typename T, int D, bool CAP>
+template <typename T, int D, bool CAP, bool UP>
 __global__ void __launch_bounds__(kThreads, 1)
     pva_prefill_pair_kernel(AttnParams p, const __grid_constant__ CUtensorMap tmap_q,
                             const __grid_constant__ CUtensorMap tmap_k,
@@ -168,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->drain, 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_half[t], 128);
       mbar_init(&bars->p_full[t], 128);
       mbar_init(&bars->o_ready[t], 1);
       mbar_init(&bars->o_free[t], 128);
@@ -219,9 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Items are drawn from a device-wide counter (zeroed by the scheduler):
       // a CTA takes the next item of the longest-first list when it is ready
       // for one, which balances uneven item costs across the persistent grid.
+      // The next index is taken as soon as the current item is decoded, so
+      // the atomic's round trip overlaps the current item's loads.
       int* next_item = p.ws + WsLayout{p.B, p.Hkv}.counters();
-      for (int idx = atomicAdd(next_item, 1); ok && idx < h.n_items; idx = atomicAdd(next_item, 1)) {
+      for (int idx = atomicAdd(next_item, 1), idx_next; ok && idx < h.n_items; idx = idx_next) {
         const PrefillItem it = decode_prefill_item(p, h, idx);
+        idx_next = idx + 1 < h.n_items ? atomicAdd(next_item, 1) : h.n_items;
         const int hi = item_key_extent(it, h.tile_tokens, p.is_causal);
         ItemSlot v;
         v.q_start = it.q_start;
@@ -276,91 +286,109 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16<T>(kTcRows, BN, false, false);
-      constexpr uint32_t idesc_o = idesc_f16<T>(kTcRows, D, false, true);
-      const uint32_t sQ = smem_u32(smem + C::OFF_Q);
-      const uint32_t sRing = smem_u32(smem + C::OFF_RING);
-      uint32_t items = 0, loads = 0, tiles = 0, taken = 0;
-      bool ok = true;
-      auto issue_s = [&](int t, uint32_t kslot) {
-        const uint32_t q_a = sQ + t * C::Q_TILE;
-        const uint32_t k_a = sRing + kslot * C::KV_TILE;
+    // The whole warp runs the loop and waits; one elected lane issues.
+    const bool leader = elect_sync();
+    constexpr uint32_t idesc_s = idesc_f16<T>(kTcRows, BN, false, false);
+    constexpr uint32_t idesc_o = idesc_f16<T>(kTcRows, D, false, true);
+    // Base descriptors, built once: the issue loops only add constants.
+    const uint64_t qdesc = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+    const uint64_t kdesc = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
+    const uint64_t vdesc = sdesc_sw128(smem_u32(smem + C::OFF_RING), C::KV_CHUNK, 1024);
+    uint32_t items = 0, loads = 0, tiles = 0, taken = 0;
+    bool ok = true;
+    auto commit = [&](uint64_t* bar) {
+      if (leader) mma_commit(bar);
+    };
+    auto issue_s = [&](int t, uint32_t kslot) {
+      const uint64_t qa = sdesc_advance(qdesc, t * C::Q_TILE);
+      const uint64_t ka = sdesc_advance(kdesc, kslot * C::KV_TILE);
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;
-          mma_ss(tmem + C::COL_S + t * 128,
-                 sdesc_sw128(q_a + (kk >> 2) * C::Q_CHUNK + off, 16, 1024),
-                 sdesc_sw128(k_a + (kk >> 2) * C::KV_CHUNK + off, 16, 1024), idesc_s,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::COL_S + t * 128, sdesc_advance(qa, (kk >> 2) * C::Q_CHUNK + off),
+                 sdesc_advance(ka, (kk >> 2) * C::KV_CHUNK + off), idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->s_full[t]);
-      };
-      auto issue_pv = [&](int t, uint32_t vslot, bool first) {
-        const uint32_t v_a = sRing + vslot * C::KV_TILE;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + C::COL_O + t * D, tmem + C::COL_S + t * 128 + kk * 8,
-                 sdesc_sw128(v_a + kk * 16 * 128, C::KV_CHUNK, 1024), idesc_o,
-                 (!first || kk > 0) ? 1u : 0u);
-        mma_commit(&bars->o_ready[t]);
-      };
-      auto wait_slot = [&](uint32_t L) -> bool {
-        const bool r = mbar_wait(&bars->ring_full[L % C::SLOTS], (L / C::SLOTS) & 1, abort, status);
-        tc_fence_after();
-        return r;
-      };
-      while (ok) {
-        const int isl = taken % kItemSlots;
-        if (!(ok = mbar_wait(&bars->item_full[isl], (taken / kItemSlots) & 1, abort, status)))
-          break;
-        const int n = bars->items[isl].n_tiles, last = bars->items[isl].last;
-        mbar_arrive(&bars->item_empty[isl]);
-        ++taken;
-        if (last) break;
-        if (n == 0) continue;
-        if (!(ok = mbar_wait(&bars->q_full, items & 1, abort, status))) break;
-        tc_fence_after();
-        // key tile j lives in load slots (loads + 2j) (K) and (loads + 2j + 1) (V)
-        if (!(ok = wait_slot(loads))) break;
-        issue_s(0, loads % C::SLOTS);
-        issue_s(1, loads % C::SLOTS);
-        mma_commit(&bars->ring_empty[loads % C::SLOTS]);
-        if (n == 1) mma_commit(&bars->q_empty);
-        for (int j = 0; ok && j < n; ++j) {
-          const uint32_t Lk = loads + 2 * j, Lv = Lk + 1, Lk1 = Lk + 2;
-          const uint32_t T_ = tiles + j;
-          // PV0(j)
-          if (j == 0 && !(ok = mbar_wait(&bars->o_free[0], (items & 1) ^ 1, abort, status))) break;
-          if (!(ok = mbar_wait(&bars->p_full[0], T_ & 1, abort, status))) break;
-          if (!(ok = wait_slot(Lv))) break;
-          issue_pv(0, Lv % C::SLOTS, j == 0);
-          // S0(j+1)
-          if (j + 1 < n) {
-            if (!(ok = wait_slot(Lk1))) break;
-            issue_s(0, Lk1 % C::SLOTS);
-          }
-          // PV1(j)
-          if (j == 0 && !(ok = mbar_wait(&bars->o_free[1], (items & 1) ^ 1, abort, status))) break;
-          if (!(ok = mbar_wait(&bars->p_full[1], T_ & 1, abort, status))) break;
-          tc_fence_after();
-          issue_pv(1, Lv % C::SLOTS, j == 0);
-          mma_commit(&bars->ring_empty[Lv % C::SLOTS]);
-          // S1(j+1)
-          if (j + 1 < n) {
-            issue_s(1, Lk1 % C::SLOTS);
-            mma_commit(&bars->ring_empty[Lk1 % C::SLOTS]);
-            if (j + 2 == n) mma_commit(&bars->q_empty);
-          }
-        }
-        loads += 2 * n;
-        tiles += n;
-        ++items;
       }
-      // Drain: all issued MMAs complete before TMEM is released.
-      mma_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, abort, status);
+    };
+    // P.V for keys [16 k0, 16 k1) of the tile (P columns 8 k0 .. 8 k1)
+    auto issue_pv = [&](int t, uint32_t vslot, bool first, int k0, int k1) {
+      const uint64_t va = sdesc_advance(vdesc, vslot * C::KV_TILE);
+      if (leader) {
+#pragma unroll
+        for (int kk = k0; kk < k1; ++kk)
+          mma_ts(tmem + C::COL_O + t * D, tmem + C::COL_S + t * 128 + kk * 8,
+                 sdesc_advance(va, kk * 16 * 128), idesc_o, (!first || kk > 0) ? 1u : 0u);
+        if (k1 == BN / 16) mma_commit(&bars->o_ready[t]);
+      }
+    };
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, status));
+    };
+    auto wait_slot = [&](uint32_t L) -> bool {
+      const bool r = wait(&bars->ring_full[L % C::SLOTS], (L / C::SLOTS) & 1);
+      tc_fence_after();
+      return r;
+    };
+    // P.V of tile t in two halves, each after its half of P has been written
+    auto pv_halves = [&](int t, uint32_t vslot, bool first, uint32_t T_) -> bool {
+      if (!wait(&bars->p_half[t], T_ & 1)) return false;
+      tc_fence_after();
+      issue_pv(t, vslot, first, 0, BN / 32);
+      if (!wait(&bars->p_full[t], T_ & 1)) return false;
+      tc_fence_after();
+      issue_pv(t, vslot, first, BN / 32, BN / 16);
+      return true;
+    };
+    while (ok) {
+      const int isl = taken % kItemSlots;
+      if (!(ok = wait(&bars->item_full[isl], (taken / kItemSlots) & 1))) break;
+      const int n = bars->items[isl].n_tiles, last = bars->items[isl].last;
+      __syncwarp();
+      if (leader) mbar_arrive(&bars->item_empty[isl]);
+      ++taken;
+      if (last) break;
+      if (n == 0) continue;
+      if (!(ok = wait(&bars->q_full, items & 1))) break;
+      tc_fence_after();
+      // key tile j lives in load slots (loads + 2j) (K) and (loads + 2j + 1) (V)
+      if (!(ok = wait_slot(loads))) break;
+      issue_s(0, loads % C::SLOTS);
+      issue_s(1, loads % C::SLOTS);
+      commit(&bars->ring_empty[loads % C::SLOTS]);
+      if (n == 1) commit(&bars->q_empty);
+      for (int j = 0; ok && j < n; ++j) {
+        const uint32_t Lk = loads + 2 * j, Lv = Lk + 1, Lk1 = Lk + 2;
+        const uint32_t T_ = tiles + j;
+        // V_j and K_{j+1} have normally landed long before P0(j) is ready:
+        // wait for them first, so that nothing but the issue itself follows
+        // the P0(j) arrival.
+        if (!(ok = wait_slot(Lv))) break;
+        if (j + 1 < n && !(ok = wait_slot(Lk1))) break;
+        // PV0(j)
+        if (j == 0 && !(ok = wait(&bars->o_free[0], (items & 1) ^ 1))) break;
+        if (!(ok = pv_halves(0, Lv % C::SLOTS, j == 0, T_))) break;
+        // S0(j+1)
+        if (j + 1 < n) issue_s(0, Lk1 % C::SLOTS);
+        // PV1(j)
+        if (j == 0 && !(ok = wait(&bars->o_free[1], (items & 1) ^ 1))) break;
+        if (!(ok = pv_halves(1, Lv % C::SLOTS, j == 0, T_))) break;
+        commit(&bars->ring_empty[Lv % C::SLOTS]);
+        // S1(j+1)
+        if (j + 1 < n) {
+          issue_s(1, Lk1 % C::SLOTS);
+          commit(&bars->ring_empty[Lk1 % C::SLOTS]);
+          if (j + 2 == n) commit(&bars->q_empty);
+        }
+      }
+      loads += 2 * n;
+      tiles += n;
+      ++items;
     }
+    // Drain: all issued MMAs complete before TMEM is released.
+    commit(&bars->drain);
+    wait(&bars->drain, 0);
   } else {
     // ------------------------------------------------- softmax + epilogue
     const int tq = warp >= 6 ? 1 : 0;  // query tile of this warpgroup
@@ -371,7 +399,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float NEG_INF = __int_as_float(0xff800000);
     const float s_mul = CAP ? p.scale / p.softcap : p.scale * kLog2e;
     const float cap_mul = p.softcap * kLog2e;
-    const bool up = p.scale > 0.0f;  // direction of the (monotone) score transform
     const int span = 2 * m_tok;      // tokens per item
     uint32_t tiles = 0, taken = 0;
     bool ok = true;
@@ -419,20 +446,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // transform (scale, then optional softcap) is monotone -- increasing
         // for scale > 0, decreasing for scale < 0 -- so the row max of the
         // transformed scores is the transform of this extreme.
-        float ext = up ? NEG_INF : -NEG_INF;
+        float ext = UP ? NEG_INF : -NEG_INF;
 #pragma unroll
         for (int c = 0; c < BN; c += 64) {
           uint32_t va[32], vb[32];
           tmem_ld32(t_lane + col_s + c, va);
           tmem_ld32(t_lane + col_s + c + 32, vb);
           tmem_wait_ld();
-          if (up) {
-            ext = masked ? extreme64<true, true>(va, vb, c, lo_c, hi_c, ext)
-                         : extreme64<true, false>(va, vb, c, lo_c, hi_c, ext);
-          } else {
-            ext = masked ? extreme64<false, true>(va, vb, c, lo_c, hi_c, ext)
-                         : extreme64<false, false>(va, vb, c, lo_c, hi_c, ext);
-          }
+          ext = masked ? extreme64<UP, true>(va, vb, c, lo_c, hi_c, ext)
+                       : extreme64<UP, false>(va, vb, c, lo_c, hi_c, ext);
         }
         const float mt = (ext == NEG_INF || ext == -NEG_INF)
                              ? NEG_INF
@@ -444,21 +466,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_used = m_new;
         }
         const float m_eff = m_used == NEG_INF ? 0.0f : m_used;
-        if (j > 0) {
-          // PV of the previous tile must be complete before O is rescaled.
-          ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[tq], (T_ - 1) & 1, abort, status));
-          if (!ok) break;
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+        // O holds the P.V products of tiles < j: the P.V MMA of tile j-1 was
+        // issued before the S MMA of tile j, and tcgen05 operations of one
+        // thread complete in order, so the s_full arrival above already
+        // covers it.
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-              uint32_t v[32];
-              tmem_ld32(t_lane + col_o + c, v);
-              tmem_wait_ld();
+          for (int c = 0; c < D; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(t_lane + col_o + c, v);
+            tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-              tmem_st32(t_lane + col_o + c, v);
-            }
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st32(t_lane + col_o + c, v);
           }
         }
         // Pass 2: p = 2^(x - m), row sum, P (16-bit pairs) into TMEM over the
@@ -477,11 +497,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             exp64<T, CAP, false>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_eff, rs, pw);
           tmem_st32(t_lane + col_s + (c >> 1), pw);
+          tmem_wait_st();
+          tc_fence_before();
+          // The first half of P lets the P.V MMA start on keys [0, 64)
+          // while the second half is computed.
+          mbar_arrive(c == 0 ? &bars->p_half[tq] : &bars->p_full[tq]);
         }
-        tmem_wait_st();
         l = l * alpha + (rs.x + rs.y);
-        tc_fence_before();
-        mbar_arrive(&bars->p_full[tq]);
       }
       if (!ok) break;
 
@@ -520,11 +542,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc<C::TMEM_COLS>(tmem);
 }
 
-template <typename T, int D, bool CAP>
+template <typename T, int D, bool CAP, bool UP>
 cudaError_t launch_pair(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, int num_sms, cudaStream_t s) {
   constexpr int smem = PairCfg<D>::SMEM;
-  auto kern = pva_prefill_pair_kernel<T, D, CAP>;
+  auto kern = pva_prefill_pair_kernel<T, D, CAP, UP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return launch_dependent(kern, dim3(num_sms), dim3(kThreads), smem, s, p, tq, tk, tv);
@@ -533,8 +555,12 @@ cudaError_t launch_pair(const AttnParams& p, const CUtensorMap& tq, const CUtens
 template <typename T, int D>
 cudaError_t launch_pair_cap(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, int num_sms, cudaStream_t s) {
-  return p.softcap != 0.0f ? launch_pair<T, D, true>(p, tq, tk, tv, num_sms, s)
-                           : launch_pair<T, D, false>(p, tq, tk, tv, num_sms, s);
+  // UP: direction of the (monotone) score transform, from the sign of the scale
+  if (p.scale > 0.0f)
+    return p.softcap != 0.0f ? launch_pair<T, D, true, true>(p, tq, tk, tv, num_sms, s)
+                             : launch_pair<T, D, false, true>(p, tq, tk, tv, num_sms, s);
+  return p.softcap != 0.0f ? launch_pair<T, D, true, false>(p, tq, tk, tv, num_sms, s)
+                           : launch_pair<T, D, false, false>(p, tq, tk, tv, num_sms, s);
 }
 
 }  // namespace

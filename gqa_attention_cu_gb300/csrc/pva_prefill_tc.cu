@@ -283,77 +283,90 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16<T>(kTcRows, BN, false, false);
-      constexpr uint32_t idesc_o = idesc_f16<T>(kTcRows, D, false, true);
-      const uint32_t sQ_a = smem_u32(sQ), sRing = smem_u32(smem + C::OFF_RING);
-      uint32_t q_cnt = 0, loads = 0, gt = 0, items = 0, taken = 0;
-      bool ok = true;
-      auto wait_slot = [&](uint32_t L) -> bool {
-        const bool r = mbar_wait(&bars->ring_full[L % C::SLOTS], (L / C::SLOTS) & 1, abort, status);
-        tc_fence_after();
-        return r;
-      };
-      // S for global key tile T_ into buffer T_ & 1 from the K in load slot L
-      auto issue_s = [&](uint32_t T_, uint32_t L) {
-        const uint32_t k_a = sRing + (L % C::SLOTS) * C::KV_TILE;
+    // The whole warp runs the loop and waits; one elected lane issues.
+    const bool leader = elect_sync();
+    constexpr uint32_t idesc_s = idesc_f16<T>(kTcRows, BN, false, false);
+    constexpr uint32_t idesc_o = idesc_f16<T>(kTcRows, D, false, true);
+    // Base descriptors, built once: the issue loops only add constants.
+    const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t kdesc = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
+    const uint64_t vdesc = sdesc_sw128(smem_u32(smem + C::OFF_RING), C::KV_CHUNK, 1024);
+    uint32_t q_cnt = 0, loads = 0, gt = 0, items = 0, taken = 0;
+    bool ok = true;
+    auto commit = [&](uint64_t* bar) {
+      if (leader) mma_commit(bar);
+    };
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, status));
+    };
+    auto wait_slot = [&](uint32_t L) -> bool {
+      const bool r = wait(&bars->ring_full[L % C::SLOTS], (L / C::SLOTS) & 1);
+      tc_fence_after();
+      return r;
+    };
+    // S for global key tile T_ into buffer T_ & 1 from the K in load slot L
+    auto issue_s = [&](uint32_t T_, uint32_t L) {
+      const uint64_t ka = sdesc_advance(kdesc, (L % C::SLOTS) * C::KV_TILE);
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;
-          mma_ss(tmem + C::COL_S + (T_ & 1) * BN,
-                 sdesc_sw128(sQ_a + (kk >> 2) * C::Q_CHUNK + off, 16, 1024),
-                 sdesc_sw128(k_a + (kk >> 2) * C::KV_CHUNK + off, 16, 1024), idesc_s,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::COL_S + (T_ & 1) * BN, sdesc_advance(qdesc, (kk >> 2) * C::Q_CHUNK + off),
+                 sdesc_advance(ka, (kk >> 2) * C::KV_CHUNK + off), idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->s_full[T_ & 1]);
         mma_commit(&bars->ring_empty[L % C::SLOTS]);  // K no longer needed once done
-      };
-      while (ok) {
-        const int isl = taken % kItemSlots;
-        if (!(ok = mbar_wait(&bars->item_full[isl], (taken / kItemSlots) & 1, abort, status)))
-          break;
-        const int n = bars->items[isl].n_tiles, last = bars->items[isl].last;
-        mbar_arrive(&bars->item_empty[isl]);
-        ++taken;
-        if (last) break;
-        if (n == 0) continue;
-        if (!(ok = mbar_wait(&bars->q_full, q_cnt & 1, abort, status))) break;
+      }
+    };
+    while (ok) {
+      const int isl = taken % kItemSlots;
+      if (!(ok = wait(&bars->item_full[isl], (taken / kItemSlots) & 1))) break;
+      const int n = bars->items[isl].n_tiles, last = bars->items[isl].last;
+      __syncwarp();
+      if (leader) mbar_arrive(&bars->item_empty[isl]);
+      ++taken;
+      if (last) break;
+      if (n == 0) continue;
+      if (!(ok = wait(&bars->q_full, q_cnt & 1))) break;
+      tc_fence_after();
+      // key tile j: K in load slot loads + 2j, V in loads + 2j + 1
+      for (int j = 0; ok && j < 2 && j < n; ++j) {
+        if (!(ok = wait_slot(loads + 2 * j))) break;
+        issue_s(gt + j, loads + 2 * j);
+      }
+      if (!ok) break;
+      if (n <= 2) commit(&bars->q_empty);
+      for (int j = 0; ok && j < n; ++j) {
+        const uint32_t T_ = gt + j, Lv = loads + 2 * j + 1;
+        // V_j and K_{j+2} have normally landed before P(j) is ready: wait for
+        // them first, so that only the issue follows the P(j) arrival.
+        if (!(ok = wait_slot(Lv))) break;
+        if (j + 2 < n && !(ok = wait_slot(loads + 2 * (j + 2)))) break;
+        if (j == 0 && !(ok = wait(&bars->o_free, (items & 1) ^ 1))) break;
+        if (!(ok = wait(&bars->p_full[T_ & 1], (T_ >> 1) & 1))) break;
         tc_fence_after();
-        // key tile j: K in load slot loads + 2j, V in loads + 2j + 1
-        for (int j = 0; ok && j < 2 && j < n; ++j) {
-          if (!(ok = wait_slot(loads + 2 * j))) break;
-          issue_s(gt + j, loads + 2 * j);
-        }
-        if (!ok) break;
-        if (n <= 2) mma_commit(&bars->q_empty);
-        for (int j = 0; ok && j < n; ++j) {
-          const uint32_t T_ = gt + j, Lv = loads + 2 * j + 1;
-          if (j == 0 && !(ok = mbar_wait(&bars->o_free, (items & 1) ^ 1, abort, status))) break;
-          if (!(ok = mbar_wait(&bars->p_full[T_ & 1], (T_ >> 1) & 1, abort, status))) break;
-          if (!(ok = wait_slot(Lv))) break;
-          const uint32_t v_a = sRing + (Lv % C::SLOTS) * C::KV_TILE;
+        const uint64_t va = sdesc_advance(vdesc, (Lv % C::SLOTS) * C::KV_TILE);
+        if (leader) {
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
             mma_ts(tmem + C::COL_O, tmem + C::COL_S + (T_ & 1) * BN + kk * 8,
-                   sdesc_sw128(v_a + kk * 16 * 128, C::KV_CHUNK, 1024), idesc_o,
-                   (j > 0 || kk > 0) ? 1u : 0u);
+                   sdesc_advance(va, kk * 16 * 128), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bars->o_ready);
           mma_commit(&bars->ring_empty[Lv % C::SLOTS]);
-          if (j + 2 < n) {
-            if (!(ok = wait_slot(loads + 2 * (j + 2)))) break;
-            issue_s(T_ + 2, loads + 2 * (j + 2));
-            if (j + 3 == n) mma_commit(&bars->q_empty);
-          }
         }
-        loads += 2 * n;
-        gt += n;
-        ++q_cnt;
-        ++items;
+        if (j + 2 < n) {
+          issue_s(T_ + 2, loads + 2 * (j + 2));
+          if (j + 3 == n) commit(&bars->q_empty);
+        }
       }
-      // Drain: all issued MMAs complete before TMEM is released.
-      mma_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, abort, status);
+      loads += 2 * n;
+      gt += n;
+      ++q_cnt;
+      ++items;
     }
+    // Drain: all issued MMAs complete before TMEM is released.
+    commit(&bars->drain);
+    wait(&bars->drain, 0);
   } else {
     // ------------------------------------------------- softmax + epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may access

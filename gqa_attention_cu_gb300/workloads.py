@@ -24,7 +24,7 @@ tests use):
                      H = 8, Hkv = 1, d = dv = 256, causal, softcap 50,
                      N(0, 2).
 
-``shrink`` divides the length ranges (and caps B) to make a same-shaped
+``shrink`` divides the length ranges (``B=`` overrides the batch size) to make a same-shaped
 small case that the CPU oracle finishes quickly.
 """
 from __future__ import annotations
