@@ -265,7 +265,7 @@ int pva_forward(const void* q, const void* k, const void* v, const int32_t* cu_s
                    &num_sms);
   if (rc != PVA_OK) return rc;
 
-  CUtensorMap tq, tk, tv, dk, dvm;
+  CUtensorMap tq, tk, tv, to, dk, dvm;
   if (plan.tensor_core) {
     if ((rc = get_encoder()) != PVA_OK) return rc;
     // An empty tensor may come as NULL; its map is never used (the device
@@ -274,10 +274,12 @@ int pva_forward(const void* q, const void* k, const void* v, const int32_t* cu_s
     if (!q) q = any;
     if (!k) k = any;
     if (!v) v = any;
+    void* o = out ? out : p.ws;
     const int G = p.G, m = kTcRows / G, bn = tc_block_n(head_size);
     if ((rc = encode_map(&tq, q, dtype, head_size, num_heads, 64, G, m, true)) != PVA_OK ||
         (rc = encode_map(&tk, k, dtype, head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK ||
-        (rc = encode_map(&tv, v, dtype, v_head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK)
+        (rc = encode_map(&tv, v, dtype, v_head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK ||
+        (rc = encode_map(&to, o, dtype, v_head_size, num_heads, 64, G, m, true)) != PVA_OK)
       return rc;
     if (plan.decode) {
       const int tkeys = decode_tile_keys(head_size);
@@ -306,7 +308,7 @@ int pva_forward(const void* q, const void* k, const void* v, const int32_t* cu_s
     return PVA_OK;
   }
   e = tc_tiles_per_item(head_size) == 2
-          ? launch_prefill_pair(p, dtype, tq, tk, tv, num_sms, stream)
+          ? launch_prefill_pair(p, dtype, tq, tk, tv, to, num_sms, stream)
           : launch_prefill_tc(p, dtype, tq, tk, tv, num_sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
   prof_mark(2, stream);

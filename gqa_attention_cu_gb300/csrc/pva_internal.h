@@ -141,9 +141,11 @@ cudaError_t launch_prefill_f32(const AttnParams& p, int num_sms, cudaStream_t s)
 cudaError_t launch_prefill_tc(const AttnParams& p, int dtype, const CUtensorMap& tq,
                               const CUtensorMap& tk, const CUtensorMap& tv, int num_sms,
                               cudaStream_t s);
+// `to`: the output as [tokens, H, dv] with a {64, G, 128/G} box (epilogue
+// stores of whole query tiles).
 cudaError_t launch_prefill_pair(const AttnParams& p, int dtype, const CUtensorMap& tq,
-                                const CUtensorMap& tk, const CUtensorMap& tv, int num_sms,
-                                cudaStream_t s);
+                                const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& to, int num_sms, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, int* done, cudaStream_t s);
 cudaError_t launch_decode(const AttnParams& p, int dtype, const CUtensorMap& tk,
                           const CUtensorMap& tv, int num_sms, cudaStream_t s);

@@ -130,17 +130,19 @@ extern "C" int pva_forward_noalloc(const void* q, const void* k, const void* v,
   p.partials = reinterpret_cast<float*>(ds.base + kStatusBytes + kIntBytes);
   p.dec_cap_units = cap_units;
 
-  CUtensorMap tq, tk, tv, dk, dvm;
+  CUtensorMap tq, tk, tv, to, dk, dvm;
   if (plan.tensor_core) {
     if ((rc = get_encoder()) != PVA_OK) return rc;
     const void* any = p.ws;  // stand-in address for empty (NULL) tensors
     const void* qa = q ? q : any;
     const void* ka = k ? k : any;
     const void* va = v ? v : any;
+    const void* oa = out ? out : any;
     const int m = kTcRows / G, bn = tc_block_n(head_size);
     if ((rc = encode_map(&tq, qa, dtype, head_size, num_heads, 64, G, m, true)) != PVA_OK ||
         (rc = encode_map(&tk, ka, dtype, head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK ||
-        (rc = encode_map(&tv, va, dtype, v_head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK)
+        (rc = encode_map(&tv, va, dtype, v_head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK ||
+        (rc = encode_map(&to, oa, dtype, v_head_size, num_heads, 64, G, m, true)) != PVA_OK)
       return rc;
     if (plan.decode) {
       const int tkeys = decode_tile_keys(head_size);
@@ -159,7 +161,7 @@ extern "C" int pva_forward_noalloc(const void* q, const void* k, const void* v,
     return e == cudaSuccess ? PVA_OK : cuda_fail(e, "fp32 attention launch");
   }
   e = tc_tiles_per_item(head_size) == 2
-          ? launch_prefill_pair(p, dtype, tq, tk, tv, ds.num_sms, stream)
+          ? launch_prefill_pair(p, dtype, tq, tk, tv, to, ds.num_sms, stream)
           : launch_prefill_tc(p, dtype, tq, tk, tv, ds.num_sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
   if (plan.decode) {

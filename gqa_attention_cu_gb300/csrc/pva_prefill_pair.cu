@@ -51,10 +51,12 @@ struct PairCfg {
   static constexpr int Q_TILE = KCH * Q_CHUNK;
   static constexpr int KV_CHUNK = BN * 128;           // 16 KB
   static constexpr int KV_TILE = KCH * KV_CHUNK;
-  static constexpr int SLOTS = D == 128 ? 5 : 12;
+  static constexpr int SLOTS = D == 128 ? 4 : 10;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = 2 * Q_TILE;
-  static constexpr int OFF_BAR = OFF_RING + SLOTS * KV_TILE;
+  static constexpr int STAGE = kTcRows * 128;                // 64 output columns of a tile
+  static constexpr int OFF_STAGE = OFF_RING + SLOTS * KV_TILE;  // one buffer per query tile
+  static constexpr int OFF_BAR = OFF_STAGE + 2 * STAGE;
   static constexpr int SMEM = OFF_BAR + 1024 + 1024;  // barriers/item ring + alignment slack
   static constexpr int TMEM_COLS = 512;
   static constexpr int COL_S = 0;        // + 128 * tile
@@ -75,6 +77,7 @@ struct ItemSlot {
 struct PairBars {
   uint64_t q_full, q_empty, drain, pad;
   uint64_t s_full[2], p_half[2], p_full[2], o_ready[2], o_free[2];
+  uint64_t stage_full[2], stage_free[2];  // epilogue staging buffer hand-off
   uint64_t ring_full[kMaxSlots], ring_empty[kMaxSlots];
   uint64_t item_full[kItemSlots], item_empty[kItemSlots];
   ItemSlot items[kItemSlots];
@@ -110,37 +113,42 @@ __device__ __forceinline__ float extreme64(const uint32_t (&va)[32], const uint3
 }
 
 // p = 2^(x - m) for columns [c, c+64), x the transformed score; row sums in
-// rs; p packed as 16-bit pairs into pw.  Written as separate sweeps (all
-// exponents, then all ex2, then sums and packing) so that 64 independent
-// ex2 are in flight behind each other.
+// rs; p packed as 16-bit pairs into pw.  Each group of 16 columns is done in
+// sweeps -- all exponents, then all ex2, then sums and packing -- so that 16
+// independent ex2 are issued back to back rather than each waiting for the
+// one before it.
 template <typename T, bool CAP, bool MASKED>
 __device__ __forceinline__ void exp64(const uint32_t (&va)[32], const uint32_t (&vb)[32], int c,
                                       int lo_c, int hi_c, float s_mul, float cap_mul, float m_eff,
                                       float2& rs, uint32_t (&pw)[32]) {
   const float2 mul2 = make_float2(s_mul, s_mul), neg_m = make_float2(-m_eff, -m_eff);
-  float2 x[32];
-#pragma unroll
-  for (int e = 0; e < 64; e += 2) {
-    const float2 sc = make_float2(col_val(va, vb, e), col_val(va, vb, e + 1));
-    if (CAP) {
-      x[e >> 1].x = cap_mul * tanh_via_exp2(sc.x * s_mul) - m_eff;
-      x[e >> 1].y = cap_mul * tanh_via_exp2(sc.y * s_mul) - m_eff;
-    } else {
-      x[e >> 1] = ffma2(sc, mul2, neg_m);
-    }
-    if (MASKED) {
-      const float ninf = __int_as_float(0xff800000);
-      x[e >> 1].x = (c + e >= lo_c && c + e < hi_c) ? x[e >> 1].x : ninf;
-      x[e >> 1].y = (c + e + 1 >= lo_c && c + e + 1 < hi_c) ? x[e >> 1].y : ninf;
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < 32; ++k) x[k] = make_float2(ex2_approx(x[k].x), ex2_approx(x[k].y));
+  const float ninf = __int_as_float(0xff800000);
   float2 acc[2] = {rs, make_float2(0.0f, 0.0f)};  // two independent partial sums
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    acc[k & 1] = fadd2(acc[k & 1], x[k]);
-    pw[k] = pack2<T>(x[k].x, x[k].y);
+  for (int g = 0; g < 32; g += 8) {
+    float2 x[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int e = 2 * (g + k);
+      const float2 sc = make_float2(col_val(va, vb, e), col_val(va, vb, e + 1));
+      if (CAP) {
+        x[k].x = cap_mul * tanh_via_exp2(sc.x * s_mul) - m_eff;
+        x[k].y = cap_mul * tanh_via_exp2(sc.y * s_mul) - m_eff;
+      } else {
+        x[k] = ffma2(sc, mul2, neg_m);
+      }
+      if (MASKED) {
+        x[k].x = (c + e >= lo_c && c + e < hi_c) ? x[k].x : ninf;
+        x[k].y = (c + e + 1 >= lo_c && c + e + 1 < hi_c) ? x[k].y : ninf;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = make_float2(ex2_approx(x[k].x), ex2_approx(x[k].y));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      acc[k & 1] = fadd2(acc[k & 1], x[k]);
+      pw[g + k] = pack2<T>(x[k].x, x[k].y);
+    }
   }
   rs = fadd2(acc[0], acc[1]);
 }
@@ -149,7 +157,8 @@ template <typename T, int D, bool CAP, bool UP>
 __global__ void __launch_bounds__(kThreads, 1)
     pva_prefill_pair_kernel(AttnParams p, const __grid_constant__ CUtensorMap tmap_q,
                             const __grid_constant__ CUtensorMap tmap_k,
-                            const __grid_constant__ CUtensorMap tmap_v) {
+                            const __grid_constant__ CUtensorMap tmap_v,
+                            const __grid_constant__ CUtensorMap tmap_o) {
   using C = PairCfg<D>;
   constexpr int BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
@@ -178,6 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->p_full[t], 128);
       mbar_init(&bars->o_ready[t], 1);
       mbar_init(&bars->o_free[t], 128);
+      mbar_init(&bars->stage_full[t], 128);
+      mbar_init(&bars->stage_free[t], 1);
     }
     for (int s = 0; s < C::SLOTS; ++s) {
       mbar_init(&bars->ring_full[s], 1);
@@ -199,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensor_map(&tmap_q);
     prefetch_tensor_map(&tmap_k);
     prefetch_tensor_map(&tmap_v);
+    prefetch_tensor_map(&tmap_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -400,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float s_mul = CAP ? p.scale / p.softcap : p.scale * kLog2e;
     const float cap_mul = p.softcap * kLog2e;
     const int span = 2 * m_tok;      // tokens per item
-    uint32_t tiles = 0, taken = 0;
+    uint32_t tiles = 0, taken = 0, stages = 0;
     bool ok = true;
     T* out = static_cast<T*>(p.out);
 
@@ -513,27 +525,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+      // A tile whose m tokens all belong to this item goes out through shared
+      // memory and one TMA store per 64 columns; otherwise (the last tile of
+      // a sequence) each thread stores its own row.
+      const int tok0 = it.q0 + tq * m_tok;
+      const int own_lo = it.q_start + first, own_hi = it.q_start + min(first + span, it.lq);
+      const bool whole = tok0 >= own_lo && tok0 + m_tok <= own_hi;
+      uint8_t* stage = smem + C::OFF_STAGE + tq * C::STAGE;
+      const bool issuer = r == 0;  // lane 0 of the warp with lane quarter 0
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(t_lane + col_o + c, v);
-        tmem_wait_ld();
-        if (own) {
+      for (int c = 0; c < D; c += 64) {
+        uint32_t w[32];  // the row's 64 values of columns [c, c + 64), packed
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 w;
-            w.x = pack2<T>(__uint_as_float(v[e + 0]) * inv, __uint_as_float(v[e + 1]) * inv);
-            w.y = pack2<T>(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
-            w.z = pack2<T>(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
-            w.w = pack2<T>(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
-            *reinterpret_cast<uint4*>(out + orow + c + e) = w;
+        for (int hh = 0; hh < 64; hh += 32) {
+          uint32_t v[32];
+          tmem_ld32(t_lane + col_o + c + hh, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            w[(hh + e) >> 1] = pack2<T>(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
+        }
+        if (whole) {
+          // The staging buffer is free once the previous store has read it.
+          if (issuer) {
+            bulk_wait_read_all();
+            mbar_arrive(&bars->stage_free[tq]);
           }
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->stage_free[tq], stages & 1, abort, status));
+          if (!ok) break;
+          // Row r: 128 bytes in the 128-byte swizzled layout of the TMA box.
+          if (r < G * m_tok) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<uint4*>(stage + r * 128 + ((u ^ (r & 7)) << 4)) =
+                  make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&bars->stage_full[tq]);
+          if (issuer) {
+            if (!(ok = mbar_wait(&bars->stage_full[tq], stages & 1, abort, status))) break;
+            tma_store_3d(&tmap_o, stage, c, it.unit * G, tok0);
+            bulk_commit();
+          }
+          ++stages;
+        } else if (own) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(out + orow + c + 8 * u) =
+                make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
       }
+      if (!ok) break;
       tc_fence_before();
       mbar_arrive(&bars->o_free[tq]);
       tiles += n;
     }
+    // Output stores must be complete before the CTA's shared memory goes.
+    if (r == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -544,38 +592,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <typename T, int D, bool CAP, bool UP>
 cudaError_t launch_pair(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                        const CUtensorMap& tv, int num_sms, cudaStream_t s) {
+                        const CUtensorMap& tv, const CUtensorMap& to, int num_sms,
+                        cudaStream_t s) {
   constexpr int smem = PairCfg<D>::SMEM;
   auto kern = pva_prefill_pair_kernel<T, D, CAP, UP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_dependent(kern, dim3(num_sms), dim3(kThreads), smem, s, p, tq, tk, tv);
+  return launch_dependent(kern, dim3(num_sms), dim3(kThreads), smem, s, p, tq, tk, tv, to);
 }
 
 template <typename T, int D>
 cudaError_t launch_pair_cap(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, int num_sms, cudaStream_t s) {
+                            const CUtensorMap& tv, const CUtensorMap& to, int num_sms,
+                            cudaStream_t s) {
   // UP: direction of the (monotone) score transform, from the sign of the scale
   if (p.scale > 0.0f)
-    return p.softcap != 0.0f ? launch_pair<T, D, true, true>(p, tq, tk, tv, num_sms, s)
-                             : launch_pair<T, D, false, true>(p, tq, tk, tv, num_sms, s);
-  return p.softcap != 0.0f ? launch_pair<T, D, true, false>(p, tq, tk, tv, num_sms, s)
-                           : launch_pair<T, D, false, false>(p, tq, tk, tv, num_sms, s);
+    return p.softcap != 0.0f ? launch_pair<T, D, true, true>(p, tq, tk, tv, to, num_sms, s)
+                             : launch_pair<T, D, false, true>(p, tq, tk, tv, to, num_sms, s);
+  return p.softcap != 0.0f ? launch_pair<T, D, true, false>(p, tq, tk, tv, to, num_sms, s)
+                           : launch_pair<T, D, false, false>(p, tq, tk, tv, to, num_sms, s);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_pair(const AttnParams& p, int dtype, const CUtensorMap& tq,
-                                const CUtensorMap& tk, const CUtensorMap& tv, int num_sms,
-                                cudaStream_t s) {
+                                const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& to, int num_sms, cudaStream_t s) {
   const bool bf = dtype == PVA_BF16;
   switch (p.d) {
     case 64:
-      return bf ? launch_pair_cap<__nv_bfloat16, 64>(p, tq, tk, tv, num_sms, s)
-                : launch_pair_cap<__half, 64>(p, tq, tk, tv, num_sms, s);
+      return bf ? launch_pair_cap<__nv_bfloat16, 64>(p, tq, tk, tv, to, num_sms, s)
+                : launch_pair_cap<__half, 64>(p, tq, tk, tv, to, num_sms, s);
     case 128:
-      return bf ? launch_pair_cap<__nv_bfloat16, 128>(p, tq, tk, tv, num_sms, s)
-                : launch_pair_cap<__half, 128>(p, tq, tk, tv, num_sms, s);
+      return bf ? launch_pair_cap<__nv_bfloat16, 128>(p, tq, tk, tv, to, num_sms, s)
+                : launch_pair_cap<__half, 128>(p, tq, tk, tv, to, num_sms, s);
     default:
       return cudaErrorInvalidValue;
   }
