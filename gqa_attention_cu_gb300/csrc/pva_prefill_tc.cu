@@ -71,7 +71,7 @@ struct ItemSlot {
 };
 
 struct Bars {
-  uint64_t q_full, q_empty, o_ready, o_free, drain, pad;
+  uint64_t q_full, q_empty, o_ready, o_done, o_free, drain;
   uint64_t s_full[2], p_full[2];
   uint64_t ring_full[8], ring_empty[8];
   uint64_t item_full[kItemSlots], item_empty[kItemSlots];
@@ -176,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
     mbar_init(&bars->o_ready, 1);
+    mbar_init(&bars->o_done, 1);
     mbar_init(&bars->o_free, 128);
     mbar_init(&bars->drain, 1);
     for (int b = 0; b < 2; ++b) {
@@ -351,7 +352,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < BN / 16; ++kk)
             mma_ts(tmem + C::COL_O, tmem + C::COL_S + (T_ & 1) * BN + kk * 8,
                    sdesc_advance(va, kk * 16 * 128), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          // o_ready completes per key tile (waited only before a rescale of
+          // O), o_done once per item.
           mma_commit(&bars->o_ready);
+          if (j + 1 == n) mma_commit(&bars->o_done);
           mma_commit(&bars->ring_empty[Lv % C::SLOTS]);
         }
         if (j + 2 < n) {
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float s_mul = CAP ? p.scale / p.softcap : p.scale * kLog2e;
     const float cap_mul = p.softcap * kLog2e;
     const bool up = p.scale > 0.0f;  // direction of the (monotone) score transform
-    uint32_t gt = 0, taken = 0;
+    uint32_t gt = 0, taken = 0, done = 0;  // done: items with key tiles
     bool ok = true;
     T* out = static_cast<T*>(p.out);
 
@@ -459,21 +463,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P (16-bit pairs) over the S buffer's first 32 columns
         tmem_st32(t_lane + col_s, pw);
         l = l * alpha + rs;
-        if (j > 0) {
-          // O must hold PV(j-1) before it is rescaled (and before PV(j)).
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+          // O must hold PV(j-1) before it is rescaled.  S(j) was issued after
+          // PV(j-2), so at most PV(j-1) is outstanding and the parity of its
+          // phase is unambiguous.  P.V(j) itself needs no wait: it reads the
+          // other S buffer and its MMAs follow P.V(j-1) in issue order.
           ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready, (T_ - 1) & 1, abort, status));
           if (!ok) break;
           tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-              uint32_t v[32];
-              tmem_ld32(t_lane + C::COL_O + c, v);
-              tmem_wait_ld();
+          for (int c = 0; c < D; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(t_lane + C::COL_O + c, v);
+            tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-              tmem_st32(t_lane + C::COL_O + c, v);
-            }
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st32(t_lane + C::COL_O + c, v);
           }
         }
         tmem_wait_st();
@@ -483,8 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // epilogue: O / l -> out (rows of this item only)
-      const uint32_t T_last = gt + n - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready, T_last & 1, abort, status));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done, done & 1, abort, status));
+      ++done;
       if (!ok) break;
       tc_fence_after();
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
