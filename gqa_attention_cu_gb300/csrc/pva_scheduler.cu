@@ -16,7 +16,7 @@
 //   * zeroed split-completion counters for the decode combine, and zeroed
 //     work counters from which the persistent compute kernels draw items.
 //
-// One CTA of 1024 threads.  B <= 2048 sequences are sorted in shared memory
+// One CTA of 128, 512 or 1024 threads (by B).  B <= 2048 sequences are sorted in shared memory
 // (bitonic); larger batches keep their input order.
 #include <limits.h>
 
@@ -26,11 +26,12 @@ namespace pva {
 
 namespace {
 
-constexpr int kThreads = 1024;
 
-// Exclusive scan of one int64 per thread across the CTA; returns the
-// exclusive prefix and writes the CTA total to *total.
+// Exclusive scan of one int64 per thread across the CTA of NT threads;
+// returns the exclusive prefix and writes the CTA total to *total.
+template <int NT>
 __device__ long long block_exclusive_scan(long long v, long long* scratch, long long* total) {
+  constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   long long x = v;
 #pragma unroll
@@ -41,7 +42,7 @@ __device__ long long block_exclusive_scan(long long v, long long* scratch, long 
   if (lane == 31) scratch[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    long long w = scratch[lane];
+    long long w = lane < NW ? scratch[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       long long y = __shfl_up_sync(0xffffffffu, w, o);
@@ -51,15 +52,16 @@ __device__ long long block_exclusive_scan(long long v, long long* scratch, long 
   }
   __syncthreads();
   const long long warp_base = warp ? scratch[warp - 1] : 0;
-  const long long tot = scratch[31];
+  const long long tot = scratch[NW - 1];
   __syncthreads();
   *total = tot;
   return warp_base + x - v;
 }
 
+template <int NT>
 __device__ long long block_sum(long long v, long long* scratch) {
   long long t;
-  block_exclusive_scan(v, scratch, &t);
+  block_exclusive_scan<NT>(v, scratch, &t);
   return t;
 }
 
@@ -88,9 +90,13 @@ __device__ __forceinline__ int decode_splits(int lkv, int chunk) {
 
 // Builds one ordered list (class 0 = prefill, 1 = decode) and its prefix.
 // Returns false when the work count overflows int32.
+// When the batch is staged (B <= kSortMax) the sorted list is also kept in
+// shared memory (s_order), so the prefix pass never reads back global memory.
+template <int NT>
 __device__ bool build_list(const AttnParams& p, const SchedConfig& c, const Lengths& seq_lens,
                            int cls, int chunk, int32_t* order, int32_t* prefix, int* n_out,
-                           int* total_out, unsigned long long* keys, long long* scratch) {
+                           int* total_out, unsigned long long* keys, int32_t* s_order,
+                           long long* scratch) {
   const int B = p.B;
   auto member = [&](int b) -> bool {
     SeqLens s = seq_lens(b);
@@ -109,7 +115,7 @@ __device__ bool build_list(const AttnParams& p, const SchedConfig& c, const Leng
   if (B <= kSortMax) {
     int N = 1;
     while (N < B) N <<= 1;
-    for (int i = threadIdx.x; i < N; i += kThreads) {
+    for (int i = threadIdx.x; i < N; i += NT) {
       unsigned long long key = ~0ull;
       if (i < B && member(i)) {
         SeqLens s = seq_lens(i);
@@ -120,7 +126,7 @@ __device__ bool build_list(const AttnParams& p, const SchedConfig& c, const Leng
     __syncthreads();
     for (int k = 2; k <= N; k <<= 1) {
       for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int i = threadIdx.x; i < N; i += kThreads) {
+        for (int i = threadIdx.x; i < N; i += NT) {
           const int ixj = i ^ j;
           if (ixj > i) {
             const unsigned long long a = keys[i], bb = keys[ixj];
@@ -135,51 +141,58 @@ __device__ bool build_list(const AttnParams& p, const SchedConfig& c, const Leng
       }
     }
     long long cnt = 0;
-    for (int i = threadIdx.x; i < B; i += kThreads) {
+    for (int i = threadIdx.x; i < B; i += NT) {
       const bool valid = keys[i] != ~0ull;
-      order[i] = valid ? (int32_t)(keys[i] & 0xffffffffu) : -1;
+      const int32_t o = valid ? (int32_t)(keys[i] & 0xffffffffu) : -1;
+      order[i] = o;
+      s_order[i] = o;
       cnt += valid;
     }
-    n = (int)block_sum(cnt, scratch);
+    n = (int)block_sum<NT>(cnt, scratch);
   } else {
     // Input order: compact the members with a scan over contiguous chunks.
-    const int per = (B + kThreads - 1) / kThreads;
+    const int per = (B + NT - 1) / NT;
     const int lo = min(B, (int)threadIdx.x * per), hi = min(B, lo + per);
     long long local = 0;
     for (int b = lo; b < hi; ++b) local += member(b);
     long long total;
-    long long pos = block_exclusive_scan(local, scratch, &total);
+    long long pos = block_exclusive_scan<NT>(local, scratch, &total);
     for (int b = lo; b < hi; ++b)
       if (member(b)) order[pos++] = b;
     __syncthreads();
     n = (int)total;
-    for (int i = n + threadIdx.x; i < B; i += kThreads) order[i] = -1;
+    for (int i = n + threadIdx.x; i < B; i += NT) order[i] = -1;
   }
   __syncthreads();
 
   // Prefix of work counts in list order: contiguous chunk per thread.
-  const int per = (n + kThreads - 1) / kThreads;
+  const int32_t* lst = B <= kSortMax ? s_order : order;
+  const int per = (n + NT - 1) / NT;
   const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
   long long local = 0;
-  for (int i = lo; i < hi; ++i) local += work(order[i]);
+  for (int i = lo; i < hi; ++i) local += work(lst[i]);
   long long total;
-  long long run = block_exclusive_scan(local, scratch, &total);
+  long long run = block_exclusive_scan<NT>(local, scratch, &total);
   const bool fits = total <= (long long)INT_MAX;
   if (fits) {
     for (int i = lo; i < hi; ++i) {
       prefix[i] = (int32_t)run;
-      run += work(order[i]);
+      run += work(lst[i]);
     }
-    for (int i = n + threadIdx.x; i <= B; i += kThreads) prefix[i] = (int32_t)total;
+    for (int i = n + threadIdx.x; i <= B; i += NT) prefix[i] = (int32_t)total;
   }
   *n_out = n;
   *total_out = fits ? (int)total : 0;
   return fits;
 }
 
-__global__ void __launch_bounds__(kThreads) pva_schedule_kernel(AttnParams p, SchedConfig c) {
+// NT threads: the smallest of 128, 512, 1024 that covers B (a small batch
+// does not pay for 32 warps walking through every barrier and scan).
+template <int NT>
+__global__ void __launch_bounds__(NT) pva_schedule_kernel(AttnParams p, SchedConfig c) {
   __shared__ unsigned long long keys[kSortMax];
   __shared__ int s_lq[kSortMax], s_lkv[kSortMax];
+  __shared__ int32_t s_order[kSortMax];
   __shared__ long long scratch[32];
   __shared__ uint32_t s_status;
   __shared__ int s_chunk;
@@ -195,6 +208,9 @@ __global__ void __launch_bounds__(kThreads) pva_schedule_kernel(AttnParams p, Sc
   const bool staged = B <= kSortMax;
   const Lengths seq_lens{p.cu_q, p.cu_kv, staged ? s_lq : nullptr, staged ? s_lkv : nullptr};
 
+  if (threadIdx.x == 0) s_status = 0;
+  __syncthreads();
+  // One pass over the offsets (all loads in flight together).
   if (threadIdx.x == 0) {
     uint32_t st = 0;
     if (p.cu_q[0] != 0) st |= PVA_DEV_CU_Q_START;
@@ -202,10 +218,9 @@ __global__ void __launch_bounds__(kThreads) pva_schedule_kernel(AttnParams p, Sc
     // Empty tensors may come as NULL; a NULL with a nonzero extent may not.
     if ((!p.q || !p.out) && p.cu_q[B] != 0) st |= PVA_DEV_NULL_TENSOR;
     if ((!p.k || !p.v) && p.cu_kv[B] != 0) st |= PVA_DEV_NULL_TENSOR;
-    s_status = st;
+    if (st) atomicOr(&s_status, st);
   }
-  __syncthreads();
-  for (int b = threadIdx.x; b < B; b += kThreads) {
+  for (int b = threadIdx.x; b < B; b += NT) {
     const int lq = p.cu_q[b + 1] - p.cu_q[b];
     const int lkv = p.cu_kv[b + 1] - p.cu_kv[b];
     if (lq < 0) atomicOr(&s_status, PVA_DEV_CU_Q_ORDER);
@@ -217,7 +232,7 @@ __global__ void __launch_bounds__(kThreads) pva_schedule_kernel(AttnParams p, Sc
   }
   // Completion counters of the decode combine start at zero every call.
   int32_t* done = ws + L.dec_done();
-  for (long long i = threadIdx.x; i < (long long)B * p.Hkv; i += kThreads) done[i] = 0;
+  for (long long i = threadIdx.x; i < (long long)B * p.Hkv; i += NT) done[i] = 0;
   if (threadIdx.x < 4) ws[L.counters() + threadIdx.x] = 0;  // work counters of this call
   __syncthreads();
 
@@ -227,15 +242,15 @@ __global__ void __launch_bounds__(kThreads) pva_schedule_kernel(AttnParams p, Sc
     // than the workspace holds (all sequences unsplit if it must).
     if (c.decode_enabled) {
       long long keyrows = 0, cnt = 0;
-      for (int b = threadIdx.x; b < B; b += kThreads) {
+      for (int b = threadIdx.x; b < B; b += NT) {
         SeqLens s = seq_lens(b);
         if (s.lq == 1) {
           keyrows += s.lkv;
           cnt += 1;
         }
       }
-      keyrows = block_sum(keyrows, scratch) * p.Hkv;
-      cnt = block_sum(cnt, scratch);
+      keyrows = block_sum<NT>(keyrows, scratch) * p.Hkv;
+      cnt = block_sum<NT>(cnt, scratch);
       long long target = (long long)c.num_sms * 8;
       long long chunk = (keyrows + target - 1) / target;
       chunk = ((chunk + 63) / 64) * 64;
@@ -244,7 +259,7 @@ __global__ void __launch_bounds__(kThreads) pva_schedule_kernel(AttnParams p, Sc
       for (int it = 0; it < 40; ++it) {
         long long units = 0;
         int any_split = 0;
-        for (int b = threadIdx.x; b < B; b += kThreads) {
+        for (int b = threadIdx.x; b < B; b += NT) {
           SeqLens s = seq_lens(b);
           if (s.lq == 1) {
             int sp = decode_splits(s.lkv, chunk > INT_MAX ? INT_MAX : (int)chunk);
@@ -252,8 +267,8 @@ __global__ void __launch_bounds__(kThreads) pva_schedule_kernel(AttnParams p, Sc
             any_split |= sp > 1;
           }
         }
-        units = block_sum(units, scratch);
-        const long long splits = block_sum(any_split, scratch);
+        units = block_sum<NT>(units, scratch);
+        const long long splits = block_sum<NT>(any_split, scratch);
         if (splits == 0 || units <= p.dec_cap_units) break;
         chunk *= 2;
       }
@@ -264,11 +279,11 @@ __global__ void __launch_bounds__(kThreads) pva_schedule_kernel(AttnParams p, Sc
     }
     __syncthreads();
     const int chunk = s_chunk;
-    bool ok = build_list(p, c, seq_lens, 0, chunk, ws + L.pref_order(), ws + L.pref_prefix(),
-                         &n_pref, &n_items, keys, scratch);
+    bool ok = build_list<NT>(p, c, seq_lens, 0, chunk, ws + L.pref_order(), ws + L.pref_prefix(),
+                         &n_pref, &n_items, keys, s_order, scratch);
     __syncthreads();
-    ok = build_list(p, c, seq_lens, 1, chunk, ws + L.dec_order(), ws + L.dec_prefix(), &n_dec,
-                    &n_units, keys, scratch) && ok;
+    ok = build_list<NT>(p, c, seq_lens, 1, chunk, ws + L.dec_order(), ws + L.dec_prefix(), &n_dec,
+                    &n_units, keys, s_order, scratch) && ok;
     if (!ok) {
       if (threadIdx.x == 0) atomicOr(&s_status, PVA_DEV_TOO_MANY);
     }
@@ -293,7 +308,12 @@ __global__ void __launch_bounds__(kThreads) pva_schedule_kernel(AttnParams p, Sc
 }  // namespace
 
 cudaError_t launch_scheduler(const AttnParams& p, const SchedConfig& c, cudaStream_t s) {
-  pva_schedule_kernel<<<1, kThreads, 0, s>>>(p, c);
+  if (p.B <= 128)
+    pva_schedule_kernel<128><<<1, 128, 0, s>>>(p, c);
+  else if (p.B <= 512)
+    pva_schedule_kernel<512><<<1, 512, 0, s>>>(p, c);
+  else
+    pva_schedule_kernel<1024><<<1, 1024, 0, s>>>(p, c);
   return cudaGetLastError();
 }
 
