@@ -3,8 +3,8 @@
 One step = one pva_forward (scheduler + prefill + decode kernels) over one
 packed batch of the named workload, inputs resident in HBM.  Default
 workload: bf16 causal GQA prefill, B=16, L_q=L_kv~U[128,2048], H=32, Hkv=8,
-d=dv=128 (metric: TFLOP/s counting only unmasked (q,k) pairs at 4*H*d FLOPs
-each).  The decode workload reports KV-read GB/s instead.
+d=dv=128 (metric: TFLOP/s counting only unmasked (q,k) pairs at 2*H*(d+dv)
+FLOPs each, 4*H*d when d == dv).  The decode workload reports KV-read GB/s instead.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl reference]
@@ -37,6 +37,8 @@ WORKLOAD_TEXT = {
     "bf16_longctx": "bf16 long-context MQA + softcap 50: B=4, L~logU[8192,32768], H=8, Hkv=1, "
                     "d=dv=256, causal, N(0,2)",
     "fp32_small": "fp32 non-causal: L={17,64,1,130}, H=Hkv=4, d=dv=64, scale 1/8",
+    "bf16_mla": "bf16 causal prefill, q.k wider than v: B=8, L_q=L_kv~U[512,4096], H=Hkv=32, "
+                "d=192, dv=128, N(0,1)",
 }
 METRIC = "varlen attn TFLOP/s (prefill) & KV-read GB/s (decode), % of roofline"
 L2_FLUSH_BYTES = 256 << 20
@@ -66,7 +68,9 @@ def unmasked_pairs(lq, lkv, is_causal: bool) -> int:
 def work_units(w):
     """Algorithmic work of one step: (FLOPs, KV bytes)."""
     pairs = unmasked_pairs(w["lq"], w["lkv"], w["is_causal"])
-    flops = pairs * 4 * w["num_heads"] * w["head_size"]
+    # 2 FLOP per multiply-add: q.k over d and p.v over dv for every unmasked
+    # (query, key) pair and head (4 H d when d == dv)
+    flops = pairs * 2 * w["num_heads"] * (w["head_size"] + w["v_head_size"])
     kv_bytes = sum(w["lkv"]) * w["kv_num_heads"] * (w["head_size"] + w["v_head_size"]) * \
         (2 if w["dtype"] != "f32" else 4)
     return flops, kv_bytes
@@ -252,7 +256,7 @@ class OracleSampler:
             # count each K/V row once per kv head, as the GPU arm does
             kv = pairs / (sp.num_heads // sp.kv_num_heads) * (sp.head_size + sp.v_head_size) * 2
             return kv / secs / 1e9, "GB/s"
-        return pairs * 4 * sp.head_size / secs / 1e12, "TFLOP/s"
+        return pairs * 2 * (sp.head_size + sp.v_head_size) / secs / 1e12, "TFLOP/s"
 
 
 def run_reference(args, w_name):
@@ -431,7 +435,9 @@ def main():
                 "frac": achieved / peaks[key],
                 "traffic": recorded_traffic(f"prefill_{w_name}"),
                 "kernel": ("pva_prefill_f32_kernel" if w["dtype"] == "f32" else
-                           "pva_prefill_pair_kernel" if w["head_size"] <= 128 else "pva_prefill_tc_kernel"),
+                           "pva_prefill_pair_kernel"
+                           if w["head_size"] == w["v_head_size"] and w["head_size"] in (64, 128)
+                           else "pva_prefill_tc_kernel"),
                 "peak_source": peaks["source"] + " " + key + " (burst: kernel timed alone)"}
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,

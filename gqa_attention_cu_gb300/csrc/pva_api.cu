@@ -137,16 +137,21 @@ int check_and_plan(const void* q, const void* k, const void* v, const int32_t* c
       return fail(PVA_ERR_UNSUPPORTED, "f32 path supports head sizes up to 256");
     plan->sched = SchedConfig{kF32TileTokens, H, kF32KeyTile, 0, 0};
   } else {
-    if (d != dv || (d != 64 && d != 128 && d != 256))
+    const bool shape_ok = (d == dv && (d == 64 || d == 96 || d == 128 || d == 192 || d == 256)) ||
+                          (d == 192 && dv == 128);
+    if (!shape_ok)
       return fail(PVA_ERR_UNSUPPORTED,
-                  "f16/bf16 path supports head_size == v_head_size in {64, 128, 256}");
+                  "f16/bf16 path supports (head_size, v_head_size) in {(64,64), (96,96), "
+                  "(128,128), (192,192), (256,256), (192,128)}");
     if (G > kTcRows)
       return fail(PVA_ERR_UNSUPPORTED, "f16/bf16 path supports num_heads/kv_num_heads <= 128");
     const uintptr_t mis = (uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)out;
     if (mis & 15) return fail(PVA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
     plan->tensor_core = true;
-    plan->decode = (G == 1 || G == 2 || G == 4 || G == 8);
-    plan->sched = SchedConfig{(kTcRows / G) * tc_tiles_per_item(d), Hkv, tc_block_n(d),
+    // The split-KV decode kernel covers d == dv in {64, 128, 256}; other
+    // shapes take their single-row sequences through the prefill kernel.
+    plan->decode = (G == 1 || G == 2 || G == 4 || G == 8) && d == dv && (d == 64 || d == 128 || d == 256);
+    plan->sched = SchedConfig{(kTcRows / G) * tc_tiles_per_item(d, dv), Hkv, tc_block_n(d, dv),
                               plan->decode ? 1 : 0, 0};
   }
   const WsLayout L{B, Hkv};
@@ -275,7 +280,7 @@ int pva_forward(const void* q, const void* k, const void* v, const int32_t* cu_s
     if (!k) k = any;
     if (!v) v = any;
     void* o = out ? out : p.ws;
-    const int G = p.G, m = kTcRows / G, bn = tc_block_n(head_size);
+    const int G = p.G, m = kTcRows / G, bn = tc_block_n(head_size, v_head_size);
     if ((rc = encode_map(&tq, q, dtype, head_size, num_heads, 64, G, m, true)) != PVA_OK ||
         (rc = encode_map(&tk, k, dtype, head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK ||
         (rc = encode_map(&tv, v, dtype, v_head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK ||
@@ -307,7 +312,7 @@ int pva_forward(const void* q, const void* k, const void* v, const int32_t* cu_s
     prof_mark(2, stream);
     return PVA_OK;
   }
-  e = tc_tiles_per_item(head_size) == 2
+  e = tc_paired(head_size, v_head_size)
           ? launch_prefill_pair(p, dtype, tq, tk, tv, to, num_sms, stream)
           : launch_prefill_tc(p, dtype, tq, tk, tv, num_sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");

@@ -26,10 +26,13 @@ constexpr int kDecodeMaxGroup = 8;  // largest H/Hkv served by the split-KV deco
 constexpr int kSortMax = 2048;      // sequences sorted on device; more keep input order
 
 // Query tiles per prefill work item: two 128-row tiles share each K/V tile
-// for d <= 128 (paired kernel); one tile for d = 256 (TMEM holds one 256-wide O).
-__host__ __device__ constexpr int tc_tiles_per_item(int D) { return D >= 256 ? 1 : 2; }
-// Keys per tensor-core key/value tile for head size D.
-__host__ __device__ constexpr int tc_block_n(int D) { return D >= 256 ? 64 : 128; }
+// in the paired kernel; one tile otherwise (TMEM holds one wide O).
+// The paired kernel (two query tiles per item) takes d == dv in {64, 128};
+// every other tensor-core shape runs one tile per item.
+__host__ __device__ constexpr bool tc_paired(int d, int dv) { return d == dv && (d == 64 || d == 128); }
+__host__ __device__ constexpr int tc_tiles_per_item(int d, int dv) { return tc_paired(d, dv) ? 2 : 1; }
+// Keys per tensor-core key/value tile.
+__host__ __device__ constexpr int tc_block_n(int d, int dv) { return tc_paired(d, dv) ? 128 : 64; }
 // Keys per decode key/value tile for head size D (16 KB of K per tile).
 __host__ __device__ constexpr int decode_tile_keys(int D) { return 8192 / D; }
 

@@ -138,7 +138,7 @@ extern "C" int pva_forward_noalloc(const void* q, const void* k, const void* v,
     const void* ka = k ? k : any;
     const void* va = v ? v : any;
     const void* oa = out ? out : any;
-    const int m = kTcRows / G, bn = tc_block_n(head_size);
+    const int m = kTcRows / G, bn = tc_block_n(head_size, v_head_size);
     if ((rc = encode_map(&tq, qa, dtype, head_size, num_heads, 64, G, m, true)) != PVA_OK ||
         (rc = encode_map(&tk, ka, dtype, head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK ||
         (rc = encode_map(&tv, va, dtype, v_head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK ||
@@ -160,7 +160,7 @@ extern "C" int pva_forward_noalloc(const void* q, const void* k, const void* v,
     e = launch_prefill_f32(p, ds.num_sms, stream);
     return e == cudaSuccess ? PVA_OK : cuda_fail(e, "fp32 attention launch");
   }
-  e = tc_tiles_per_item(head_size) == 2
+  e = tc_paired(head_size, v_head_size)
           ? launch_prefill_pair(p, dtype, tq, tk, tv, to, ds.num_sms, stream)
           : launch_prefill_tc(p, dtype, tq, tk, tv, ds.num_sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");

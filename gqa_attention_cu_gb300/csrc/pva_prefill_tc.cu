@@ -1,6 +1,9 @@
 // bf16/f16 prefill on the 5th-generation tensor cores (tcgen05 + TMEM) with
-// TMA-staged operands for head size d = dv = 256 (one 128-row query tile per
-// CTA: the 256-column O accumulator leaves TMEM room for one tile only).
+// TMA-staged operands, one 128-row query tile per CTA, for the head sizes the
+// paired kernel does not take: (d, dv) = (256, 256), (192, 192), (192, 128)
+// (q.k wider than v, as in multi-head latent attention) and (96, 96).  A head
+// size that is not a multiple of 64 is loaded in 64-column boxes whose tail
+// lies outside the tensor and reads the TMA zero fill; the MMAs never touch it.
 //
 // The arithmetic is the page's (packed_varlen_attention.rs, stages 1-5:
 // scale * q.k, optional softcap * tanh(score / softcap) before the mask, the
@@ -22,8 +25,8 @@
 //               feeds O += P V with A taken from TMEM; S(j+2) reuses the buffer
 //               after that MMA (tcgen05 MMAs of one thread run in issue order).
 //   warps 2..5  softmax / correction / epilogue, one thread per TMEM lane.
-// TMEM: S buffers [0,64) and [64,128), O [128,384).  Shared memory: Q 64 KB +
-// 5 K/V slots of 32 KB.
+// TMEM: S buffers [0,64) and [64,128), O [128,128+dv).  Shared memory (d = dv
+// = 256): Q 64 KB + 5 K/V slots of 32 KB.
 //
 // Softcap: tanh(t) of the scaled score t = s * scale / softcap comes from its
 // Maclaurin series t - t^3/3 + 2t^5/15 - 17t^7/315 + 62t^9/2835 -
@@ -43,14 +46,18 @@ constexpr int kItemSlots = 4;
 constexpr int kSoftmaxWarps = 4;
 constexpr float kPolyLimit = 0.5f;          // |t| range of the tanh series
 
-template <int D>
+template <int DQK, int DV>
 struct TcCfg {
+  static_assert(DQK % 16 == 0 && DV % 32 == 0 && DQK <= 256 && DV <= 256, "head sizes");
   static constexpr int BN = 64;
-  static constexpr int KCH = D / 64;              // 128-byte column chunks of a row
+  static constexpr int KCH = (DQK + 63) / 64;     // 128-byte column chunks of a q/k row
+  static constexpr int VCH = (DV + 63) / 64;      // the same for a v row
   static constexpr int Q_CHUNK = kTcRows * 128;   // bytes of one chunk of the Q tile
   static constexpr int Q_BYTES = KCH * Q_CHUNK;
   static constexpr int KV_CHUNK = BN * 128;       // bytes of one chunk of a K or V tile
-  static constexpr int KV_TILE = KCH * KV_CHUNK;
+  static constexpr int K_BYTES = KCH * KV_CHUNK;
+  static constexpr int V_BYTES = VCH * KV_CHUNK;
+  static constexpr int KV_TILE = K_BYTES > V_BYTES ? K_BYTES : V_BYTES;  // one ring slot
   static constexpr int SLOTS = 5;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = Q_BYTES;
@@ -59,7 +66,7 @@ struct TcCfg {
   static constexpr int TMEM_COLS = 512;
   static constexpr int COL_S = 0;                 // + BN * buffer
   static constexpr int COL_O = 2 * BN;
-  static_assert(2 * BN + D <= TMEM_COLS, "TMEM budget");
+  static_assert(2 * BN + DV <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448 - 64, "shared memory budget");
 };
 
@@ -148,12 +155,12 @@ __device__ __forceinline__ float exp64(const uint32_t (&va)[32], const uint32_t 
   return r.x + r.y;
 }
 
-template <typename T, int D, bool CAP>
+template <typename T, int DQK, int DV, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     pva_prefill_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap tmap_q,
                           const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v) {
-  using C = TcCfg<D>;
+  using C = TcCfg<DQK, DV>;
   constexpr int BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -262,9 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  status)))
               break;
             uint8_t* dst = smem + C::OFF_RING + sl * C::KV_TILE;
-            mbar_arrive_expect_tx(&bars->ring_full[sl], (uint32_t)C::KV_TILE);
-#pragma unroll
-            for (int c = 0; c < C::KCH; ++c)
+            mbar_arrive_expect_tx(&bars->ring_full[sl], (uint32_t)(kv ? C::V_BYTES : C::K_BYTES));
+            const int nch = kv ? C::VCH : C::KCH;
+            for (int c = 0; c < nch; ++c)
               tma_load_3d(dst + c * C::KV_CHUNK, kv ? &tmap_v : &tmap_k, &bars->ring_full[sl],
                           c * 64, g, k0);
           }
@@ -287,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp runs the loop and waits; one elected lane issues.
     const bool leader = elect_sync();
     constexpr uint32_t idesc_s = idesc_f16<T>(kTcRows, BN, false, false);
-    constexpr uint32_t idesc_o = idesc_f16<T>(kTcRows, D, false, true);
+    constexpr uint32_t idesc_o = idesc_f16<T>(kTcRows, DV, false, true);
     // Base descriptors, built once: the issue loops only add constants.
     const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t kdesc = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t ka = sdesc_advance(kdesc, (L % C::SLOTS) * C::KV_TILE);
       if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;
           mma_ss(tmem + C::COL_S + (T_ & 1) * BN, sdesc_advance(qdesc, (kk >> 2) * C::Q_CHUNK + off),
                  sdesc_advance(ka, (kk >> 2) * C::KV_CHUNK + off), idesc_s, kk > 0 ? 1u : 0u);
@@ -399,11 +406,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i = tok - it.q_start;  // its local query position
       const int first = it.t * m_tok;
       const bool own = r < G * m_tok && i >= first && i < min(first + m_tok, it.lq);
-      const size_t orow = ((size_t)tok * p.H + (size_t)it.unit * G + (r % G)) * D;
+      const size_t orow = ((size_t)tok * p.H + (size_t)it.unit * G + (r % G)) * DV;
       if (n == 0) {
         if (own) {
 #pragma unroll
-          for (int c = 0; c < D; c += 8)
+          for (int c = 0; c < DV; c += 8)
             *reinterpret_cast<uint4*>(out + orow + c) = make_uint4(0, 0, 0, 0);
         }
         continue;
@@ -472,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
+          for (int c = 0; c < DV; c += 32) {
             uint32_t v[32];
             tmem_ld32(t_lane + C::COL_O + c, v);
             tmem_wait_ld();
@@ -494,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
+      for (int c = 0; c < DV; c += 32) {
         uint32_t v[32];
         tmem_ld32(t_lane + C::COL_O + c, v);
         tmem_wait_ld();
@@ -522,21 +529,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc<C::TMEM_COLS>(tmem);
 }
 
-template <typename T, int D, bool CAP>
+template <typename T, int DQK, int DV, bool CAP>
 cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                       const CUtensorMap& tv, int num_sms, cudaStream_t s) {
-  constexpr int smem = TcCfg<D>::SMEM;
-  auto kern = pva_prefill_tc_kernel<T, D, CAP>;
+  constexpr int smem = TcCfg<DQK, DV>::SMEM;
+  auto kern = pva_prefill_tc_kernel<T, DQK, DV, CAP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return launch_dependent(kern, dim3(num_sms), dim3(kThreads), smem, s, p, tq, tk, tv);
 }
 
-template <typename T>
+template <typename T, int DQK, int DV>
 cudaError_t launch_tc_cap(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, int num_sms, cudaStream_t s) {
-  return p.softcap != 0.0f ? launch_tc<T, 256, true>(p, tq, tk, tv, num_sms, s)
-                           : launch_tc<T, 256, false>(p, tq, tk, tv, num_sms, s);
+  return p.softcap != 0.0f ? launch_tc<T, DQK, DV, true>(p, tq, tk, tv, num_sms, s)
+                           : launch_tc<T, DQK, DV, false>(p, tq, tk, tv, num_sms, s);
+}
+
+template <typename T>
+cudaError_t launch_tc_shape(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, int num_sms, cudaStream_t s) {
+  if (p.d == 256 && p.dv == 256) return launch_tc_cap<T, 256, 256>(p, tq, tk, tv, num_sms, s);
+  if (p.d == 192 && p.dv == 192) return launch_tc_cap<T, 192, 192>(p, tq, tk, tv, num_sms, s);
+  if (p.d == 192 && p.dv == 128) return launch_tc_cap<T, 192, 128>(p, tq, tk, tv, num_sms, s);
+  if (p.d == 96 && p.dv == 96) return launch_tc_cap<T, 96, 96>(p, tq, tk, tv, num_sms, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -544,9 +561,8 @@ cudaError_t launch_tc_cap(const AttnParams& p, const CUtensorMap& tq, const CUte
 cudaError_t launch_prefill_tc(const AttnParams& p, int dtype, const CUtensorMap& tq,
                               const CUtensorMap& tk, const CUtensorMap& tv, int num_sms,
                               cudaStream_t s) {
-  if (p.d != 256) return cudaErrorInvalidValue;
-  return dtype == PVA_BF16 ? launch_tc_cap<__nv_bfloat16>(p, tq, tk, tv, num_sms, s)
-                           : launch_tc_cap<__half>(p, tq, tk, tv, num_sms, s);
+  return dtype == PVA_BF16 ? launch_tc_shape<__nv_bfloat16>(p, tq, tk, tv, num_sms, s)
+                           : launch_tc_shape<__half>(p, tq, tk, tv, num_sms, s);
 }
 
 }  // namespace pva

@@ -23,6 +23,8 @@ tests use):
 * ``bf16_longctx`` : B = 4, L_q = L_kv = round(exp(U(ln 8192, ln 32768))),
                      H = 8, Hkv = 1, d = dv = 256, causal, softcap 50,
                      N(0, 2).
+* ``bf16_mla``     : B = 8, L_q = L_kv ~ U{512..4096}, H = Hkv = 32,
+                     d = 192, dv = 128 (q.k wider than v), causal, N(0, 1).
 
 ``shrink`` divides the length ranges (``B=`` overrides the batch size) to make a same-shaped
 small case that the CPU oracle finishes quickly.
@@ -69,6 +71,8 @@ WORKLOADS = {
                             "decode", params={"lo": 512, "hi": 8192}),
     "bf16_longctx": Workload("bf16_longctx", 4, 8, 1, 256, 256, "bf16", True, 0.0, 50.0,
                              math.sqrt(2.0), "loguniform_self", params={"lo": 8192, "hi": 32768}),
+    "bf16_mla": Workload("bf16_mla", 8, 32, 32, 192, 128, "bf16", True, 0.0, 0.0, 1.0,
+                         "uniform_self", params={"lo": 512, "hi": 4096}),
 }
 
 

@@ -79,8 +79,9 @@ typedef enum { PVA_F32 = 0, PVA_F16 = 1, PVA_BF16 = 2 } pva_dtype;
  *                `out` is left untouched (see pva_get_status).
  * B            : number of sequences, >= 1.  Empty sequences are allowed.
  * num_heads, kv_num_heads : H >= 1 and Hkv >= 1 with H % Hkv == 0.
- * head_size, v_head_size  : d and dv.  f16/bf16: d == dv in {64, 128, 256}
- *                and H / Hkv <= 128.  f32: 1 <= d, dv <= 256.
+ * head_size, v_head_size  : d and dv.  f16/bf16: (d, dv) in {(64, 64),
+ *                (96, 96), (128, 128), (192, 192), (256, 256), (192, 128)} and
+ *                H / Hkv <= 128.  f32: 1 <= d, dv <= 256.
  * scale        : finite; 0 selects the default 1/sqrt(head_size) (computed in
  *                fp32).  Any other value is used as given.
  * is_causal    : nonzero selects the tail-aligned causal mask.

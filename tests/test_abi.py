@@ -63,7 +63,8 @@ def _call(lib, **kw):
     (dict(B=0), -1), (dict(H=0), -1), (dict(Hkv=0), -1), (dict(H=6, Hkv=4), -1),
     (dict(dtype=3), -1), (dict(dtype=-1), -1),
     (dict(scale=float("nan")), -1), (dict(softcap=float("inf")), -1),
-    (dict(d=96, dv=96), -2), (dict(d=128, dv=64), -2), (dict(dtype=0, d=512, dv=64), -2),
+    (dict(d=80, dv=80), -2), (dict(d=128, dv=64), -2), (dict(d=192, dv=96), -2),
+    (dict(dtype=0, d=512, dv=64), -2),
     (dict(H=256, Hkv=1), -2), (dict(q=24), -1),
 ])
 def test_host_argument_checks_need_no_gpu(lib, kw, code):

@@ -70,7 +70,8 @@ def test_fp32_small_workload_full():
 
 
 @pytest.mark.parametrize("name,shrink", [("bf16_prefill", 4), ("bf16_chunked", 4),
-                                         ("bf16_decode", 8), ("bf16_longctx", 16)])
+                                         ("bf16_decode", 8), ("bf16_longctx", 16),
+                                         ("bf16_mla", 8)])
 def test_bf16_workloads_shrunk_full(name, shrink):
     w = workloads.make(name, shrink=shrink)
     out = run_gpu(w["q"], w["k"], w["v"], w["cu_q"], w["cu_kv"], w["num_heads"],
@@ -100,6 +101,28 @@ def test_group_sizes_not_dividing_the_tile(G):
 @pytest.mark.parametrize("causal", [False, True])
 def test_f16(causal):
     parity([100, 37, 260], [140, 37, 260], 16, 4, 128, "f16", causal=causal, seed=5)
+
+
+# Head sizes of the single-tile kernel beyond 256: 96 (loaded in 64-column
+# boxes with a zero-filled tail), 192, and q.k wider than v (192/128).
+@pytest.mark.parametrize("d,dv", [(96, 96), (192, 192), (192, 128)])
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_prefill_extra_head_sizes(d, dv, G):
+    Hkv = 2
+    lq, lkv = [1, 200, 77, 3, 130], [1, 260, 300, 3, 130]
+    q, k, v, cq, ck = workloads.make_packed(lq, lkv, G * Hkv, Hkv, d, dv, "bf16", seed=d + dv + G)
+    out = run_gpu(q, k, v, cq, ck, G * Hkv, Hkv, 0.0, True, 0.0)
+    check(out, oracle.attention(q, k, v, cq, ck, G * Hkv, Hkv, 0.0, True, 0.0), "bf16")
+
+
+@pytest.mark.parametrize("d,dv,dtype,causal,softcap", [(96, 96, "f16", False, 0.0),
+                                                      (192, 128, "bf16", True, 30.0),
+                                                      (192, 128, "f16", False, 0.0)])
+def test_prefill_extra_head_sizes_variants(d, dv, dtype, causal, softcap):
+    lq, lkv = [64, 1, 129, 300], [64, 700, 200, 300]
+    q, k, v, cq, ck = workloads.make_packed(lq, lkv, 8, 2, d, dv, dtype, sigma=1.5, seed=7)
+    out = run_gpu(q, k, v, cq, ck, 8, 2, 0.0, causal, softcap)
+    check(out, oracle.attention(q, k, v, cq, ck, 8, 2, 0.0, causal, softcap), dtype)
 
 
 @pytest.mark.parametrize("d,dv", [(64, 64), (32, 48), (128, 96), (8, 256), (256, 16)])
@@ -307,13 +330,16 @@ def test_malformed_offsets_latch_status_and_write_nothing(bad):
 # ---------------------------------------------------------------------------
 # Scheduler: bit-exact against a host mirror
 # ---------------------------------------------------------------------------
-def sched_mirror(lq, lkv, H, Hkv, d, dtype, num_sms):
+def sched_mirror(lq, lkv, H, Hkv, d, dtype, num_sms, dv=None):
     B = len(lq)
+    dv = d if dv is None else dv
     if dtype == 0:
         tile, units, dec = 16, H, False
     else:
         G = H // Hkv
-        tile, units, dec = (128 // G) * (1 if d >= 256 else 2), Hkv, G in (1, 2, 4, 8)
+        paired = d == dv and d in (64, 128)
+        tile, units = (128 // G) * (2 if paired else 1), Hkv
+        dec = G in (1, 2, 4, 8) and d == dv and d in (64, 128, 256)
     cap = min(B * Hkv * 16, 16384)
     INT_MAX = 2 ** 31 - 1
     chunk = INT_MAX
@@ -359,10 +385,11 @@ def sched_mirror(lq, lkv, H, Hkv, d, dtype, num_sms):
 
 
 @pytest.mark.parametrize("seed", range(6))
-@pytest.mark.parametrize("cfg", [(32, 8, 128, 2), (8, 1, 256, 2), (6, 2, 64, 1), (4, 4, 64, 0),
-                                 (64, 2, 128, 2)])
+@pytest.mark.parametrize("cfg", [(32, 8, 128, 128, 2), (8, 1, 256, 256, 2), (6, 2, 64, 64, 1),
+                                 (4, 4, 64, 64, 0), (64, 2, 128, 128, 2), (16, 4, 192, 128, 2),
+                                 (8, 2, 96, 96, 1)])
 def test_scheduler_matches_host_mirror(seed, cfg):
-    H, Hkv, d, dtype = cfg
+    H, Hkv, d, dv, dtype = cfg
     g = torch.Generator().manual_seed(seed)
     B = int(torch.randint(1, 300, (1,), generator=g))
     lq = torch.randint(0, 600, (B,), generator=g)
@@ -370,9 +397,9 @@ def test_scheduler_matches_host_mirror(seed, cfg):
     lkv = (torch.tensor(lq) + torch.randint(0, 9000, (B,), generator=g)).tolist()
     dev = torch.device("cuda:0")
     words = pva.pva_schedule(workloads.cu_from_lengths(lq).to(dev),
-                             workloads.cu_from_lengths(lkv).to(dev), B, H, Hkv, d, d, 1, dtype)
+                             workloads.cu_from_lengths(lkv).to(dev), B, H, Hkv, d, dv, 1, dtype)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert words == sched_mirror(lq, lkv, H, Hkv, d, dtype, sms)
+    assert words == sched_mirror(lq, lkv, H, Hkv, d, dtype, sms, dv)
 
 
 def test_scheduler_configs_match_host_mirror():
@@ -385,7 +412,7 @@ def test_scheduler_configs_match_host_mirror():
                                  workloads.cu_from_lengths(lkv).to(dev), len(lq), w.num_heads,
                                  w.kv_num_heads, w.head_size, w.v_head_size, int(w.is_causal), dt)
         assert words == sched_mirror(lq, lkv, w.num_heads, w.kv_num_heads, w.head_size, dt,
-                                     sms), name
+                                     sms, w.v_head_size), name
 
 
 # ---------------------------------------------------------------------------
@@ -402,7 +429,8 @@ def _sub_batch(w, seqs):
             workloads.cu_from_lengths([w["lkv"][b] for b in seqs]))
 
 
-@pytest.mark.parametrize("name", ["bf16_prefill", "bf16_chunked", "bf16_decode", "bf16_longctx"])
+@pytest.mark.parametrize("name", ["bf16_prefill", "bf16_chunked", "bf16_decode", "bf16_longctx",
+                                  "bf16_mla"])
 def test_full_size_workload_sampled_rows(name):
     w = workloads.make(name, device="cuda:0")
     H, Hkv, dv = w["num_heads"], w["kv_num_heads"], w["v_head_size"]
