@@ -63,6 +63,11 @@ def _bind(path: str):
     lib.pva_oracle_rows.argtypes = [dp, dp, dp, ip, ip, lp, ctypes.c_int64, dp,
                                     i, i, i, i, i, d, i, d, i]
     lib.pva_oracle_rows.restype = i
+    lib.pva_oracle_forward_window.argtypes = [dp, dp, dp, ip, ip, dp, i, i, i, i, i, d, i, d, i, i]
+    lib.pva_oracle_forward_window.restype = i
+    lib.pva_oracle_rows_window.argtypes = [dp, dp, dp, ip, ip, lp, ctypes.c_int64, dp,
+                                           i, i, i, i, i, d, i, d, i, i]
+    lib.pva_oracle_rows_window.restype = i
     lib.pva_oracle_max_threads.argtypes = []
     lib.pva_oracle_max_threads.restype = i
     return lib
@@ -131,11 +136,12 @@ def max_threads() -> int:
 
 def attention(q, k, v, cu_seqlens_q, cu_seqlens_kv, num_heads: int, kv_num_heads: int,
               scale: float = 0.0, is_causal: bool = False, softcap: float = 0.0,
-              threads: int = 0) -> np.ndarray:
+              threads: int = 0, local_window: int = 0) -> np.ndarray:
     """fp64 attention over packed sequences.
 
     q [total_q, H, d], k [total_kv, Hkv, d], v [total_kv, Hkv, dv] (any float
-    dtype, torch or numpy); cu_* int32 [B+1].  Returns float64
+    dtype, torch or numpy); cu_* int32 [B+1].  ``local_window`` > 0 also masks
+    keys before (causal limit + 1 - local_window).  Returns float64
     [total_q, H, dv].
     """
     lib = _load()
@@ -146,11 +152,14 @@ def attention(q, k, v, cu_seqlens_q, cu_seqlens_kv, num_heads: int, kv_num_heads
     d, dv = _head_dims(qd, vd, H, Hkv)
     total_q = int(cq[-1])
     out = np.zeros((total_q, H, dv), dtype=np.float64)
-    rc = lib.pva_oracle_forward(_ptr(qd, ctypes.c_double), _ptr(kd, ctypes.c_double),
-                                _ptr(vd, ctypes.c_double), _ptr(cq, ctypes.c_int32),
-                                _ptr(ck, ctypes.c_int32), _ptr(out, ctypes.c_double),
-                                B, H, Hkv, d, dv, resolve_scale(scale, d), int(bool(is_causal)),
-                                float(np.float32(softcap)), int(threads))
+    args = (_ptr(qd, ctypes.c_double), _ptr(kd, ctypes.c_double), _ptr(vd, ctypes.c_double),
+            _ptr(cq, ctypes.c_int32), _ptr(ck, ctypes.c_int32), _ptr(out, ctypes.c_double),
+            B, H, Hkv, d, dv, resolve_scale(scale, d), int(bool(is_causal)),
+            float(np.float32(softcap)))
+    if local_window:
+        rc = lib.pva_oracle_forward_window(*args, int(local_window), int(threads))
+    else:
+        rc = lib.pva_oracle_forward(*args, int(threads))
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (code {rc})")
     return out
@@ -158,7 +167,8 @@ def attention(q, k, v, cu_seqlens_q, cu_seqlens_kv, num_heads: int, kv_num_heads
 
 def attention_rows(q, k, v, cu_seqlens_q, cu_seqlens_kv, rows, num_heads: int,
                    kv_num_heads: int, scale: float = 0.0, is_causal: bool = False,
-                   softcap: float = 0.0, threads: int = 0) -> np.ndarray:
+                   softcap: float = 0.0, threads: int = 0,
+                   local_window: int = 0) -> np.ndarray:
     """fp64 attention for selected output rows only (row = token * H + head).
     Returns float64 [len(rows), dv]."""
     lib = _load()
@@ -169,12 +179,14 @@ def attention_rows(q, k, v, cu_seqlens_q, cu_seqlens_kv, rows, num_heads: int,
     H, Hkv = int(num_heads), int(kv_num_heads)
     d, dv = _head_dims(qd, vd, H, Hkv)
     out = np.zeros((r.shape[0], dv), dtype=np.float64)
-    rc = lib.pva_oracle_rows(_ptr(qd, ctypes.c_double), _ptr(kd, ctypes.c_double),
-                             _ptr(vd, ctypes.c_double), _ptr(cq, ctypes.c_int32),
-                             _ptr(ck, ctypes.c_int32), _ptr(r, ctypes.c_int64), r.shape[0],
-                             _ptr(out, ctypes.c_double), B, H, Hkv, d, dv,
-                             resolve_scale(scale, d), int(bool(is_causal)),
-                             float(np.float32(softcap)), int(threads))
+    args = (_ptr(qd, ctypes.c_double), _ptr(kd, ctypes.c_double), _ptr(vd, ctypes.c_double),
+            _ptr(cq, ctypes.c_int32), _ptr(ck, ctypes.c_int32), _ptr(r, ctypes.c_int64),
+            r.shape[0], _ptr(out, ctypes.c_double), B, H, Hkv, d, dv,
+            resolve_scale(scale, d), int(bool(is_causal)), float(np.float32(softcap)))
+    if local_window:
+        rc = lib.pva_oracle_rows_window(*args, int(local_window), int(threads))
+    else:
+        rc = lib.pva_oracle_rows(*args, int(threads))
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (code {rc})")
     return out

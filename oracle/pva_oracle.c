@@ -17,6 +17,11 @@
  *     group`).
  *   - same page, "Causal alignment": local query i sees local key j iff
  *     j <= i + (L_kv - L_q).
+ *   - attention.rs and group_query_attention.rs, the softmax / reference
+ *     kernels' `local_window`: with a window W > 0, keys before
+ *     frontier + 1 - W are masked as well (frontier = i + L_kv - L_q, the
+ *     causal limit, which sets the window's end whether or not the causal
+ *     mask itself is on).  W <= 0 means no window.
  *   - same page, kernel stages 1-5: score = scale * q.k; softcap (when
  *     nonzero) replaces the score by softcap * tanh(score / softcap) before the
  *     mask; max-subtracted exponentials, normalised; a row whose every key is
@@ -61,7 +66,7 @@ static void attend_one_row(const double* q, const double* k, const double* v,
                            int b, int64_t tok, int h,
                            int H, int Hkv, int d, int dv,
                            double scale, int is_causal, double softcap,
-                           double* scores, double* out_row) {
+                           int local_window, double* scores, double* out_row) {
   const int group = H / Hkv;
   const int g = h / group;                          /* shared key/value head */
   const int64_t q_start = cu_q[b];
@@ -78,6 +83,7 @@ static void attend_one_row(const double* q, const double* k, const double* v,
   double m = -INFINITY;
   for (int64_t j = 0; j < L_kv; ++j) {
     if (is_causal && j > frontier) { scores[j] = -INFINITY; continue; }
+    if (local_window > 0 && j < frontier + 1 - local_window) { scores[j] = -INFINITY; continue; }
     const double* krow = k + ((kv_start + j) * Hkv + g) * (int64_t)d;
     double dot = 0.0;
     for (int p = 0; p < d; ++p) dot += qrow[p] * krow[p];
@@ -128,10 +134,11 @@ static int64_t max_kv_len(const int32_t* cu_kv, int B) {
 }
 
 /* Full forward: every row of `out` [cu_q[B], H, dv] is written. */
-int pva_oracle_forward(const double* q, const double* k, const double* v,
-                       const int32_t* cu_q, const int32_t* cu_kv, double* out,
-                       int B, int H, int Hkv, int d, int dv, double scale,
-                       int is_causal, double softcap, int nthreads) {
+int pva_oracle_forward_window(const double* q, const double* k, const double* v,
+                              const int32_t* cu_q, const int32_t* cu_kv, double* out,
+                              int B, int H, int Hkv, int d, int dv, double scale,
+                              int is_causal, double softcap, int local_window,
+                              int nthreads) {
   int rc = check_args(cu_q, cu_kv, B, H, Hkv, d, dv);
   if (rc != ORACLE_OK) return rc;
   const int64_t total_q = cu_q[B];
@@ -157,21 +164,29 @@ int pva_oracle_forward(const double* q, const double* k, const double* v,
       const int h = (int)(row % H);
       const int b = owner_sequence(cu_q, B, tok);
       attend_one_row(q, k, v, cu_q, cu_kv, b, tok, h, H, Hkv, d, dv, scale,
-                     is_causal, softcap, scores, out + row * (int64_t)dv);
+                     is_causal, softcap, local_window, scores, out + row * (int64_t)dv);
     }
     free(scores);
   }
   return failed ? ORACLE_OOM : ORACLE_OK;
 }
 
+int pva_oracle_forward(const double* q, const double* k, const double* v,
+                       const int32_t* cu_q, const int32_t* cu_kv, double* out,
+                       int B, int H, int Hkv, int d, int dv, double scale,
+                       int is_causal, double softcap, int nthreads) {
+  return pva_oracle_forward_window(q, k, v, cu_q, cu_kv, out, B, H, Hkv, d, dv, scale,
+                                   is_causal, softcap, 0, nthreads);
+}
+
 /* Sampled forward: only the listed rows, row = token * H + head, written to
  * out_rows [n_rows, dv] in the order given.  Used where the full problem is
  * too large for the CPU. */
-int pva_oracle_rows(const double* q, const double* k, const double* v,
-                    const int32_t* cu_q, const int32_t* cu_kv,
-                    const int64_t* rows, int64_t n_rows, double* out_rows,
-                    int B, int H, int Hkv, int d, int dv, double scale,
-                    int is_causal, double softcap, int nthreads) {
+int pva_oracle_rows_window(const double* q, const double* k, const double* v,
+                           const int32_t* cu_q, const int32_t* cu_kv,
+                           const int64_t* rows, int64_t n_rows, double* out_rows,
+                           int B, int H, int Hkv, int d, int dv, double scale,
+                           int is_causal, double softcap, int local_window, int nthreads) {
   int rc = check_args(cu_q, cu_kv, B, H, Hkv, d, dv);
   if (rc != ORACLE_OK) return rc;
   const int64_t total_rows = (int64_t)cu_q[B] * H;
@@ -198,11 +213,20 @@ int pva_oracle_rows(const double* q, const double* k, const double* v,
       const int h = (int)(rows[r] % H);
       const int b = owner_sequence(cu_q, B, tok);
       attend_one_row(q, k, v, cu_q, cu_kv, b, tok, h, H, Hkv, d, dv, scale,
-                     is_causal, softcap, scores, out_rows + r * (int64_t)dv);
+                     is_causal, softcap, local_window, scores, out_rows + r * (int64_t)dv);
     }
     free(scores);
   }
   return failed ? ORACLE_OOM : ORACLE_OK;
+}
+
+int pva_oracle_rows(const double* q, const double* k, const double* v,
+                    const int32_t* cu_q, const int32_t* cu_kv,
+                    const int64_t* rows, int64_t n_rows, double* out_rows,
+                    int B, int H, int Hkv, int d, int dv, double scale,
+                    int is_causal, double softcap, int nthreads) {
+  return pva_oracle_rows_window(q, k, v, cu_q, cu_kv, rows, n_rows, out_rows, B, H, Hkv, d,
+                                dv, scale, is_causal, softcap, 0, nthreads);
 }
 
 /* Threads OpenMP would use by default (reported with CPU timings). */

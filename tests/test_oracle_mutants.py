@@ -37,6 +37,9 @@ MUTANTS = [
     ("kv_start_ignored", "const int64_t kv_start = cu_kv[b];", "const int64_t kv_start = cu_q[b];"),
     ("no_normalise", "const double p = scores[j] / l;", "const double p = scores[j];"),
     ("owner_off_by_one", "if ((int64_t)cu_q[mid] <= tok) lo = mid;", "if ((int64_t)cu_q[mid] < tok) lo = mid;"),
+    ("window_off_by_one", "j < frontier + 1 - local_window", "j <= frontier + 1 - local_window"),
+    ("window_from_row_not_limit", "j < frontier + 1 - local_window", "j < i + 1 - local_window"),
+    ("window_ignored", "if (local_window > 0 && j < frontier + 1 - local_window)", "if (0)"),
 ]
 
 
@@ -63,6 +66,9 @@ def _pin_checks():
         ("nonpad", lambda: [pins.test_nonpad_kv_seqlen_prefix_sum_reproduces_padded_masking(s)
                             for s in range(4)]),
         ("bruteforce", lambda: [pins.test_bruteforce_tiny_random_against_sdpa(s) for s in range(6)]),
+        ("window", lambda: ([pins.test_window_row_is_plain_attention_over_the_window_keys(s, c)
+                             for s in range(2) for c in (False, True)],
+                            pins.test_window_of_one_returns_the_value_row_at_the_causal_limit())),
         ("closed_forms", lambda: (pins.test_constant_value_rows_return_that_row(),
                                   pins.test_zero_query_gives_mean_of_visible_values(),
                                   pins.test_empty_sequences_and_fully_masked_rows_are_zero())),

@@ -352,3 +352,72 @@ def test_default_scale_is_float32_inverse_sqrt():
     assert oracle.resolve_scale(0.0, 128) == float(np.float32(1) / np.sqrt(np.float32(128)))
     assert oracle.resolve_scale(0.0, 64) == 0.125
     assert math.isclose(oracle.resolve_scale(0.0, 256), 1 / 16)
+
+
+# ---------------------------------------------------------------------------
+# Local (sliding) window: keys before causal limit + 1 - W are masked
+# (attention.rs / group_query_attention.rs `local_window`).
+# ---------------------------------------------------------------------------
+def _window_case(seed, causal):
+    g = torch.Generator().manual_seed(700 + seed)
+    B, H, Hkv, d, dv = 3, 4, 2, 8, 6
+    lkv = torch.randint(1, 14, (B,), generator=g).tolist()
+    lq = [int(torch.randint(1, L + 1, (1,), generator=g)) for L in lkv]
+    q, k, v, cq, ck = workloads.make_packed(lq, lkv, H, Hkv, d, dv, "f32", gen=g)
+    return q.double(), k.double(), v.double(), cq, ck, lq, lkv, H, Hkv, d
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("causal", [False, True])
+def test_window_row_is_plain_attention_over_the_window_keys(seed, causal):
+    """Every output row under a window W equals the un-windowed oracle run on
+    that single query row against only the keys the window leaves visible
+    (a one-row problem in which nothing else is masked)."""
+    q, k, v, cq, ck, lq, lkv, H, Hkv, d = _window_case(seed, causal)
+    for W in (1, 2, 5, 40):
+        out = oracle.attention(q, k, v, cq, ck, H, Hkv, 0.0, causal, local_window=W)
+        for b, (a, L) in enumerate(zip(lq, lkv)):
+            for i in range(a):
+                frontier = i + L - a
+                lo, hi = max(0, frontier + 1 - W), (min(L, frontier + 1) if causal else L)
+                kv0 = int(ck[b])
+                for h in range(H):
+                    got = out[int(cq[b]) + i, h]
+                    if hi <= lo:
+                        np.testing.assert_array_equal(got, 0.0)
+                        continue
+                    g_ = h // (H // Hkv)
+                    ref = oracle.attention(q[int(cq[b]) + i: int(cq[b]) + i + 1, h:h + 1],
+                                           k[kv0 + lo: kv0 + hi, g_:g_ + 1],
+                                           v[kv0 + lo: kv0 + hi, g_:g_ + 1],
+                                           torch.tensor([0, 1], dtype=torch.int32),
+                                           torch.tensor([0, hi - lo], dtype=torch.int32), 1, 1,
+                                           oracle.resolve_scale(0.0, d), False)
+                    np.testing.assert_allclose(got, ref[0, 0], rtol=0, atol=1e-12)
+
+
+def test_window_of_one_returns_the_value_row_at_the_causal_limit():
+    q, k, v, cq, ck, lq, lkv, H, Hkv, d = _window_case(9, True)
+    out = oracle.attention(q, k, v, cq, ck, H, Hkv, 0.0, True, local_window=1)
+    for b, (a, L) in enumerate(zip(lq, lkv)):
+        for i in range(a):
+            for h in range(H):
+                row = v[int(ck[b]) + i + L - a, h // (H // Hkv)].numpy()
+                np.testing.assert_allclose(out[int(cq[b]) + i, h], row, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_window_wider_than_every_sequence_changes_nothing(causal):
+    q, k, v, cq, ck, lq, lkv, H, Hkv, d = _window_case(3, causal)
+    a = oracle.attention(q, k, v, cq, ck, H, Hkv, 0.0, causal)
+    for W in (max(lkv) + max(lq), 10 ** 6):
+        np.testing.assert_array_equal(oracle.attention(q, k, v, cq, ck, H, Hkv, 0.0, causal,
+                                                       local_window=W), a)
+
+
+def test_window_rows_api_matches_full_forward():
+    q, k, v, cq, ck, lq, lkv, H, Hkv, d = _window_case(5, True)
+    full = oracle.attention(q, k, v, cq, ck, H, Hkv, 0.0, True, local_window=3)
+    rows = np.arange(full.shape[0] * H)[::3]
+    got = oracle.attention_rows(q, k, v, cq, ck, rows, H, Hkv, 0.0, True, local_window=3)
+    np.testing.assert_array_equal(got, full.reshape(-1, full.shape[-1])[rows])
