@@ -39,35 +39,34 @@ WORKLOAD_TEXT = {
     "fp32_small": "fp32 non-causal: L={17,64,1,130}, H=Hkv=4, d=dv=64, scale 1/8",
     "bf16_mla": "bf16 causal prefill, q.k wider than v: B=8, L_q=L_kv~U[512,4096], H=Hkv=32, "
                 "d=192, dv=128, N(0,1)",
+    "bf16_window": "bf16 causal GQA prefill with a local window of 4096 keys: B=4, "
+                   "L~logU[8192,32768], H=32, Hkv=8, d=dv=128, N(0,1)",
 }
 METRIC = "varlen attn TFLOP/s (prefill) & KV-read GB/s (decode), % of roofline"
 L2_FLUSH_BYTES = 256 << 20
 
 
-def unmasked_pairs(lq, lkv, is_causal: bool) -> int:
+def visible_keys(a: int, b: int, is_causal: bool, window: int = 0):
+    """Keys each of the a query rows of a sequence sees (b keys): row i, causal
+    limit c = i + b - a, sees [max(0, c + 1 - window) if window > 0 else 0,
+    min(b, c + 1) if causal else b)."""
+    import numpy as np
+    c = np.arange(a, dtype=np.int64) + (b - a)
+    hi = np.minimum(b, c + 1) if is_causal else np.full(a, b, dtype=np.int64)
+    lo = np.maximum(0, c + 1 - window) if window > 0 else np.zeros(a, dtype=np.int64)
+    return np.maximum(hi - lo, 0)
+
+
+def unmasked_pairs(lq, lkv, is_causal: bool, window: int = 0) -> int:
     """(query, key) pairs the mask leaves visible, summed over sequences (one
-    head).  Query i of a sequence sees keys j <= i + L_kv - L_q when causal."""
-    total = 0
-    for a, b in zip(lq, lkv):
-        a, b = int(a), int(b)
-        if not is_causal:
-            total += a * b
-            continue
-        off = b - a
-        lo = max(0, -off)                # first row that sees any key
-        full = max(lo, b - 1 - off)      # rows from here on see all b keys
-        hi = min(a, full)
-        if hi > lo:
-            n = hi - lo
-            total += n * (off + 1) + (lo + hi - 1) * n // 2
-        if a > full:
-            total += (a - full) * b
-    return total
+    head)."""
+    return int(sum(int(visible_keys(int(a), int(b), is_causal, window).sum())
+                   for a, b in zip(lq, lkv)))
 
 
 def work_units(w):
     """Algorithmic work of one step: (FLOPs, KV bytes)."""
-    pairs = unmasked_pairs(w["lq"], w["lkv"], w["is_causal"])
+    pairs = unmasked_pairs(w["lq"], w["lkv"], w["is_causal"], w.get("window", 0))
     # 2 FLOP per multiply-add: q.k over d and p.v over dv for every unmasked
     # (query, key) pair and head (4 H d when d == dv)
     flops = pairs * 2 * w["num_heads"] * (w["head_size"] + w["v_head_size"])
@@ -225,15 +224,14 @@ class OracleSampler:
         lq, lkv = self.lq[b], self.lkv[b]
         q, k, v, cq, ck = self.wl.make_packed([lq], [lkv], H, Hkv, sp.head_size, sp.v_head_size,
                                               sp.dtype, sp.sigma, gen=self.gen)
-        i = np.arange(lq)
-        vis = np.minimum(lkv, i + (lkv - lq) + 1) if sp.is_causal else np.full(lq, lkv)
-        vis = np.maximum(vis, 0)
+        vis = visible_keys(lq, lkv, sp.is_causal, sp.window)
         avg = max(1.0, float(vis.mean()))
         n_rows = int(max(1, min(lq * H, pair_budget / avg)))
         rows = np.sort(self.rng.choice(lq * H, size=n_rows, replace=False))
         pairs = int(vis[rows // H].sum())
         t0 = time.perf_counter()
-        oracle.attention_rows(q, k, v, cq, ck, rows, H, Hkv, sp.scale, sp.is_causal, sp.softcap)
+        oracle.attention_rows(q, k, v, cq, ck, rows, H, Hkv, sp.scale, sp.is_causal, sp.softcap,
+                              local_window=sp.window)
         return time.perf_counter() - t0, pairs, n_rows
 
     def run(self, seconds: float):
@@ -343,9 +341,16 @@ def main():
     out = torch.empty(w["q"].shape[0], H, dv, dtype=w["q"].dtype, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
+    def forward(q, k, v, cq, ck, o, s):
+        if w["window"] > 0:
+            pva.pva_forward_local(q, k, v, cq, ck, o, w["B"], H, Hkv, d, dv, w["scale"],
+                                  int(w["is_causal"]), w["softcap"], w["window"], stream=s)
+        else:
+            pva.pva_forward(q, k, v, cq, ck, o, w["B"], H, Hkv, d, dv, w["scale"],
+                            int(w["is_causal"]), w["softcap"], stream=s)
+
     def step(s):
-        pva.pva_forward(w["q"], w["k"], w["v"], w["cu_q"], w["cu_kv"], out, w["B"], H, Hkv, d,
-                        dv, w["scale"], int(w["is_causal"]), w["softcap"], stream=s)
+        forward(w["q"], w["k"], w["v"], w["cu_q"], w["cu_kv"], out, s)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -401,9 +406,7 @@ def main():
             a.record(stream)
             for k_ in host:
                 dbuf[k_].copy_(host[k_], non_blocking=True)
-            pva.pva_forward(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["cu_q"], dbuf["cu_kv"], out,
-                            w["B"], H, Hkv, d, dv, w["scale"], int(w["is_causal"]), w["softcap"],
-                            stream=stream)
+            forward(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["cu_q"], dbuf["cu_kv"], out, stream)
             out_host.copy_(out, non_blocking=True)
             b.record(stream)
             b.synchronize()

@@ -15,7 +15,7 @@ import threading
 
 from . import workloads  # noqa: F401  (seeded synthetic inputs)
 
-__all__ = ["pva_forward", "pva_get_status", "pva_schedule", "pva_status_string",
+__all__ = ["pva_forward", "pva_forward_local", "pva_get_status", "pva_schedule", "pva_status_string",
            "pva_last_error", "pva_release", "pva_version", "pva_profile", "pva_kernel_times",
            "pva_selftest_wait", "load_library", "build", "PvaError", "DTYPE_CODES", "DEV_FLAGS"]
 
@@ -57,6 +57,9 @@ def load_library(path: str | None = None):
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.pva_forward.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, f, i, vp]
         lib.pva_forward.restype = i
+        lib.pva_forward_local.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, f, i, i,
+                                          vp]
+        lib.pva_forward_local.restype = i
         lib.pva_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.pva_get_status.restype = i
         lib.pva_schedule.argtypes = [vp, vp, i, i, i, i, i, i, i,
@@ -119,6 +122,22 @@ def pva_forward(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B: int, num_heads: in
                          cu_seqlens_kv.data_ptr(), out.data_ptr(), int(B), int(num_heads),
                          int(kv_num_heads), int(head_size), int(v_head_size), float(scale),
                          int(is_causal), float(softcap), code, _stream_ptr(stream))
+    _check(rc)
+
+
+def pva_forward_local(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B: int, num_heads: int,
+                      kv_num_heads: int, head_size: int, v_head_size: int, scale: float = 0.0,
+                      is_causal: int = 0, softcap: float = 0.0, local_window: int = 0,
+                      dtype: int | None = None, stream=None) -> None:
+    """pva_forward with a local window: with local_window = W > 0 each query
+    row also ignores keys before (its causal limit + 1 - W)."""
+    lib = load_library()
+    code = _dtype_code(q) if dtype is None else int(dtype)
+    rc = lib.pva_forward_local(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                               cu_seqlens_q.data_ptr(), cu_seqlens_kv.data_ptr(), out.data_ptr(),
+                               int(B), int(num_heads), int(kv_num_heads), int(head_size),
+                               int(v_head_size), float(scale), int(is_causal), float(softcap),
+                               int(local_window), code, _stream_ptr(stream))
     _check(rc)
 
 

@@ -260,6 +260,15 @@ int pva_forward(const void* q, const void* k, const void* v, const int32_t* cu_s
                 const int32_t* cu_seqlens_kv, void* out, int B, int num_heads, int kv_num_heads,
                 int head_size, int v_head_size, float scale, int is_causal, float softcap,
                 int dtype, void* stream_) {
+  return pva_forward_local(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B, num_heads,
+                           kv_num_heads, head_size, v_head_size, scale, is_causal, softcap, 0,
+                           dtype, stream_);
+}
+
+int pva_forward_local(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                      const int32_t* cu_seqlens_kv, void* out, int B, int num_heads,
+                      int kv_num_heads, int head_size, int v_head_size, float scale,
+                      int is_causal, float softcap, int local_window, int dtype, void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   std::lock_guard<std::mutex> lock(g_mu);
   Plan plan;
@@ -269,6 +278,7 @@ int pva_forward(const void* q, const void* k, const void* v, const int32_t* cu_s
                    head_size, v_head_size, scale, is_causal, softcap, dtype, stream, &plan, &p,
                    &num_sms);
   if (rc != PVA_OK) return rc;
+  p.window = local_window > 0 ? local_window : 0;
 
   CUtensorMap tq, tk, tv, to, dk, dvm;
   if (plan.tensor_core) {

@@ -85,6 +85,7 @@ struct AttnParams {
   float scale;    // resolved (default already applied)
   float softcap;  // 0 = off
   int is_causal;
+  int window;     // local window W > 0: keys before (causal limit + 1 - W) masked; 0 = none
   uint32_t* status;   // sticky PVA_DEV_* bits (OR-ed, cleared by pva_get_status)
   int32_t* ws;        // workspace int region
   float* partials;    // decode split partials

@@ -46,8 +46,17 @@ __device__ __forceinline__ PrefillItem decode_prefill_item(const AttnParams& p,
   return r;
 }
 
-// Number of key tiles of `block_n` keys an item must visit: keys beyond the
-// causal frontier of its last query row are never loaded.
+// First local key an item must visit: 0, or with a local window W the window
+// start of its first query row (later rows start later).
+__device__ __forceinline__ int item_key_begin(const PrefillItem& it, int tile_tokens, int window) {
+  if (window <= 0) return 0;
+  const int first_row = it.t * tile_tokens;
+  const int lo = first_row + (it.lkv - it.lq) + 1 - window;
+  return lo > 0 ? lo : 0;
+}
+
+// End of the local key range an item must visit: keys beyond the causal
+// frontier of its last query row are never loaded.
 __device__ __forceinline__ int item_key_extent(const PrefillItem& it, int tile_tokens,
                                                int is_causal) {
   const int last_row = min((it.t + 1) * tile_tokens, it.lq) - 1;

@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(kWarps * 32) pva_prefill_f32_kernel(AttnParams
     const int nrows = min(kF32TileTokens, item.lq - row0);
     const int off = item.lkv - item.lq;
     const int hi = item_key_extent(item, kF32TileTokens, p.is_causal);
+    const int kb = item_key_begin(item, kF32TileTokens, p.window) / kF32KeyTile * kF32KeyTile;
 
     __syncthreads();  // previous item done with shared memory
     for (int e = threadIdx.x; e < kF32TileTokens * d; e += blockDim.x) {
@@ -63,7 +64,7 @@ __global__ void __launch_bounds__(kWarps * 32) pva_prefill_f32_kernel(AttnParams
       for (int u = 0; u < kChan; ++u) acc[r][u] = 0.0f;
     }
 
-    for (int k0 = 0; k0 < hi; k0 += kF32KeyTile) {
+    for (int k0 = kb; k0 < hi; k0 += kF32KeyTile) {
       const int nk = min(kF32KeyTile, hi - k0);
       __syncthreads();  // previous key tile consumed
       for (int e = threadIdx.x; e < kF32KeyTile * d; e += blockDim.x) {
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(kWarps * 32) pva_prefill_f32_kernel(AttnParams
         const int key = k0 + lane;
         bool visible = lane < nk;
         if (p.is_causal) visible = visible && key <= i + off;
+        if (p.window > 0) visible = visible && key >= i + off + 1 - p.window;
         float s = 0.0f;
         const float* qr = sq + lr * d;
         const float* kr = sk + lane * kstride;

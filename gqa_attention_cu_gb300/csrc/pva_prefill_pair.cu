@@ -71,7 +71,8 @@ struct ItemSlot {
   int q_start, kv_start, lq, lkv;
   int t, unit, n_tiles, q0;
   int last;  // 1: no more items for this CTA
-  int pad[3];
+  int jb;  // first key tile (a local window skips the ones before)
+  int pad[2];
 };
 
 struct PairBars {
@@ -252,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         v.lkv = it.lkv;
         v.t = it.t;
         v.unit = it.unit;
-        v.n_tiles = (hi + BN - 1) / BN;
+        v.jb = item_key_begin(it, h.tile_tokens, p.window) / BN;
+        v.n_tiles = max(0, (hi + BN - 1) / BN - v.jb);
         v.q0 = min(it.q_start + it.t * h.tile_tokens, total_q - 2 * m_tok);
         v.last = 0;
         if (!(ok = publish(v))) break;
@@ -268,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         c * 64, g * G, v.q0 + t * m_tok);
         ++items;
         for (int j = 0; ok && j < v.n_tiles; ++j) {
-          const int k0 = min(v.kv_start + j * BN, total_kv - BN);
+          const int k0 = min(v.kv_start + (v.jb + j) * BN, total_kv - BN);
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv, ++loads) {
             const int sl = loads % C::SLOTS;
@@ -442,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int off = it.lkv - it.lq;
       const int row_hi = p.is_causal ? min(it.lkv, i + off + 1) : it.lkv;
+      const int row_lo = p.window > 0 ? i + off + 1 - p.window : 0;  // local window start
       float m_used = NEG_INF, l = 0.0f;
 
       for (int j = 0; j < n; ++j) {
@@ -449,10 +452,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[tq], T_ & 1, abort, status));
         if (!ok) break;
         tc_fence_after();
-        const int k0 = min(it.kv_start + j * BN, total_kv - BN);
+        const int J = it.jb + j;            // key tile index within the sequence
+        const int k0 = min(it.kv_start + J * BN, total_kv - BN);
         const int base = k0 - it.kv_start;  // local key index of column 0
-        const int lo_c = j * BN - base;     // visible columns [lo_c, hi_c)
-        const int hi_c = min((j + 1) * BN, row_hi) - base;
+        const int lo_c = max(J * BN, row_lo) - base;  // visible columns [lo_c, hi_c)
+        const int hi_c = min((J + 1) * BN, row_hi) - base;
         const bool masked = !__all_sync(0xffffffffu, lo_c <= 0 && hi_c >= BN);
         // Pass 1: extreme raw score over the visible columns.  The score
         // transform (scale, then optional softcap) is monotone -- increasing

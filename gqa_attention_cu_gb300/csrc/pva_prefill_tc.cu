@@ -74,7 +74,8 @@ struct ItemSlot {
   int q_start, kv_start, lq, lkv;
   int t, unit, n_tiles, q0;
   int last;
-  int pad[3];
+  int jb;  // first key tile (a local window skips the ones before)
+  int pad[2];
 };
 
 struct Bars {
@@ -248,7 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         v.lkv = it.lkv;
         v.t = it.t;
         v.unit = it.unit;
-        v.n_tiles = (hi + BN - 1) / BN;
+        v.jb = item_key_begin(it, h.tile_tokens, p.window) / BN;
+        v.n_tiles = max(0, (hi + BN - 1) / BN - v.jb);
         v.q0 = min(it.q_start + it.t * h.tile_tokens, total_q - m_tok);
         v.last = 0;
         if (!(ok = publish(v))) break;
@@ -261,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sQ + c * C::Q_CHUNK, &tmap_q, &bars->q_full, c * 64, g * G, v.q0);
         ++q_cnt;
         for (int j = 0; ok && j < v.n_tiles; ++j) {
-          const int k0 = min(v.kv_start + j * BN, total_kv - BN);
+          const int k0 = min(v.kv_start + (v.jb + j) * BN, total_kv - BN);
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv, ++loads) {
             const int sl = loads % C::SLOTS;
@@ -417,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int off = it.lkv - it.lq;
       const int row_hi = p.is_causal ? min(it.lkv, i + off + 1) : it.lkv;
+      const int row_lo = p.window > 0 ? i + off + 1 - p.window : 0;  // local window start
       float m_used = NEG_INF, l = 0.0f;
 
       for (int j = 0; j < n; ++j) {
@@ -430,10 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(t_lane + col_s, va);
         tmem_ld32(t_lane + col_s + 32, vb);
         tmem_wait_ld();
-        const int k0 = min(it.kv_start + j * BN, total_kv - BN);
+        const int J = it.jb + j;            // key tile index within the sequence
+        const int k0 = min(it.kv_start + J * BN, total_kv - BN);
         const int base = k0 - it.kv_start;  // local key index of column 0
-        const int lo_c = j * BN - base;     // visible columns [lo_c, hi_c)
-        const int hi_c = min((j + 1) * BN, row_hi) - base;
+        const int lo_c = max(J * BN, row_lo) - base;  // visible columns [lo_c, hi_c)
+        const int hi_c = min((J + 1) * BN, row_hi) - base;
         const bool masked = !__all_sync(0xffffffffu, lo_c <= 0 && hi_c >= BN);
         float mx, mn;
         if (masked)

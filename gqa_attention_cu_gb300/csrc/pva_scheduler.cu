@@ -82,6 +82,12 @@ struct Lengths {
   }
 };
 
+// Keys a single-row (decode) sequence attends to: all L_kv, or the last W of
+// them under a local window W.
+__device__ __forceinline__ int decode_keys(int lkv, int window) {
+  return window > 0 && window < lkv ? window : lkv;
+}
+
 __device__ __forceinline__ int decode_splits(int lkv, int chunk) {
   if (lkv <= chunk) return 1;
   int s = (lkv + chunk - 1) / chunk;
@@ -108,7 +114,7 @@ __device__ bool build_list(const AttnParams& p, const SchedConfig& c, const Leng
     SeqLens s = seq_lens(b);
     if (cls == 0)
       return (long long)((s.lq + c.tile_tokens - 1) / c.tile_tokens) * c.units_per_tile;
-    return (long long)decode_splits(s.lkv, chunk) * p.Hkv;
+    return (long long)decode_splits(decode_keys(s.lkv, p.window), chunk) * p.Hkv;
   };
 
   int n = 0;
@@ -245,7 +251,7 @@ __global__ void __launch_bounds__(NT) pva_schedule_kernel(AttnParams p, SchedCon
       for (int b = threadIdx.x; b < B; b += NT) {
         SeqLens s = seq_lens(b);
         if (s.lq == 1) {
-          keyrows += s.lkv;
+          keyrows += decode_keys(s.lkv, p.window);
           cnt += 1;
         }
       }
@@ -262,7 +268,8 @@ __global__ void __launch_bounds__(NT) pva_schedule_kernel(AttnParams p, SchedCon
         for (int b = threadIdx.x; b < B; b += NT) {
           SeqLens s = seq_lens(b);
           if (s.lq == 1) {
-            int sp = decode_splits(s.lkv, chunk > INT_MAX ? INT_MAX : (int)chunk);
+            int sp = decode_splits(decode_keys(s.lkv, p.window),
+                                   chunk > INT_MAX ? INT_MAX : (int)chunk);
             units += (long long)sp * p.Hkv;
             any_split |= sp > 1;
           }

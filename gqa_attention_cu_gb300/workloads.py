@@ -25,6 +25,9 @@ tests use):
                      N(0, 2).
 * ``bf16_mla``     : B = 8, L_q = L_kv ~ U{512..4096}, H = Hkv = 32,
                      d = 192, dv = 128 (q.k wider than v), causal, N(0, 1).
+* ``bf16_window``  : B = 4, L_q = L_kv = round(exp(U(ln 8192, ln 32768))),
+                     H = 32, Hkv = 8, d = dv = 128, causal, local window 4096,
+                     N(0, 1).
 
 ``shrink`` divides the length ranges (``B=`` overrides the batch size) to make a same-shaped
 small case that the CPU oracle finishes quickly.
@@ -57,6 +60,7 @@ class Workload:
     fixed_lq: tuple = ()
     fixed_lkv: tuple = ()
     params: dict = field(default_factory=dict)
+    window: int = 0       # local window (pva_forward_local); 0 = none
 
 
 WORKLOADS = {
@@ -73,6 +77,8 @@ WORKLOADS = {
                              math.sqrt(2.0), "loguniform_self", params={"lo": 8192, "hi": 32768}),
     "bf16_mla": Workload("bf16_mla", 8, 32, 32, 192, 128, "bf16", True, 0.0, 0.0, 1.0,
                          "uniform_self", params={"lo": 512, "hi": 4096}),
+    "bf16_window": Workload("bf16_window", 4, 32, 8, 128, 128, "bf16", True, 0.0, 0.0, 1.0,
+                            "loguniform_self", params={"lo": 8192, "hi": 32768}, window=4096),
 }
 
 
@@ -153,5 +159,5 @@ def make(name: str, seed: int = 0, shrink: int = 1, B: int | None = None,
         "num_heads": w.num_heads, "kv_num_heads": w.kv_num_heads,
         "head_size": w.head_size, "v_head_size": w.v_head_size,
         "dtype": w.dtype, "is_causal": w.is_causal, "scale": w.scale,
-        "softcap": w.softcap, "sigma": w.sigma,
+        "softcap": w.softcap, "sigma": w.sigma, "window": w.window,
     }

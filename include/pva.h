@@ -105,6 +105,23 @@ int pva_forward(const void* q, const void* k, const void* v,
                 float softcap, int dtype, void* stream);
 
 /*
+ * pva_forward_local -- pva_forward with a local (sliding) attention window,
+ * the `local_window` of the softmax and grouped-query reference kernels on the
+ * attention.rs and group_query_attention.rs pages.  With local_window = W > 0,
+ * query row i of a sequence (causal limit c = i + L_kv - L_q) also ignores the
+ * keys j < c + 1 - W, so it sees at most the W keys ending at c (causal) or the
+ * keys [max(0, c + 1 - W), L_kv) (non-causal).  local_window <= 0 is exactly
+ * pva_forward.  Key tiles wholly before a work item's window are never loaded,
+ * and decode rows split only their last W keys.  Other arguments, errors and
+ * asynchrony: as pva_forward.
+ */
+int pva_forward_local(const void* q, const void* k, const void* v,
+                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                      void* out, int B, int num_heads, int kv_num_heads,
+                      int head_size, int v_head_size, float scale, int is_causal,
+                      float softcap, int local_window, int dtype, void* stream);
+
+/*
  * pva_forward_noalloc -- the same attention as pva_forward, for callers that
  * cannot allocate device memory when they call (a runtime whose device memory
  * is planned ahead and owned by an arena or governor, code that runs while
