@@ -91,20 +91,34 @@ __device__ __forceinline__ float col_val(const uint32_t (&va)[32], const uint32_
   return __uint_as_float(e < 32 ? va[e] : vb[e - 32]);
 }
 
+// Column masks, chosen once per tile and warp: kMaskNone (every column
+// visible), kMaskHi (visible iff col < hi_c: the causal diagonal, where no row
+// of the warp starts inside the tile) and kMaskBoth (lo_c <= col < hi_c, one
+// unsigned compare).  The column is a compile-time constant in the unrolled
+// loops, so a test is one integer compare and one select.
+constexpr int kMaskNone = 0, kMaskHi = 1, kMaskBoth = 2;
+template <int MASK>
+__device__ __forceinline__ bool col_visible(int col, int lo_c, int hi_c, unsigned span) {
+  if (MASK == kMaskNone) return true;
+  if (MASK == kMaskHi) return col < hi_c;
+  return (unsigned)(col - lo_c) < span;
+}
+
 // Extreme (max if UP, else min) of the raw scores of columns [c, c+64);
-// MASKED replaces the columns outside [lo_c, hi_c) by the neutral value.
-template <bool UP, bool MASKED>
+// a mask replaces the invisible columns by the neutral value.
+template <bool UP, int MASK>
 __device__ __forceinline__ float extreme64(const uint32_t (&va)[32], const uint32_t (&vb)[32],
                                            int c, int lo_c, int hi_c, float ext) {
   const float neutral = UP ? __int_as_float(0xff800000) : __int_as_float(0x7f800000);
+  const unsigned span = hi_c > lo_c ? (unsigned)(hi_c - lo_c) : 0u;
   // four independent partial extremes: no 32-long dependency chain
   float acc[4] = {ext, neutral, neutral, neutral};
 #pragma unroll
   for (int e = 0; e < 64; e += 2) {
     float x0 = col_val(va, vb, e), x1 = col_val(va, vb, e + 1);
-    if (MASKED) {
-      x0 = (c + e >= lo_c && c + e < hi_c) ? x0 : neutral;
-      x1 = (c + e + 1 >= lo_c && c + e + 1 < hi_c) ? x1 : neutral;
+    if (MASK != kMaskNone) {
+      x0 = col_visible<MASK>(c + e, lo_c, hi_c, span) ? x0 : neutral;
+      x1 = col_visible<MASK>(c + e + 1, lo_c, hi_c, span) ? x1 : neutral;
     }
     float& a = acc[(e >> 1) & 3];
     a = UP ? fmax3f(a, x0, x1) : fmin3f(a, x0, x1);
@@ -118,11 +132,12 @@ __device__ __forceinline__ float extreme64(const uint32_t (&va)[32], const uint3
 // sweeps -- all exponents, then all ex2, then sums and packing -- so that 16
 // independent ex2 are issued back to back rather than each waiting for the
 // one before it.
-template <typename T, bool CAP, bool MASKED>
+template <typename T, bool CAP, int MASK>
 __device__ __forceinline__ void exp64(const uint32_t (&va)[32], const uint32_t (&vb)[32], int c,
                                       int lo_c, int hi_c, float s_mul, float cap_mul, float m_eff,
                                       float2& rs, uint32_t (&pw)[32]) {
   const float2 mul2 = make_float2(s_mul, s_mul), neg_m = make_float2(-m_eff, -m_eff);
+  const unsigned span = hi_c > lo_c ? (unsigned)(hi_c - lo_c) : 0u;
   const float ninf = __int_as_float(0xff800000);
   float2 acc[2] = {rs, make_float2(0.0f, 0.0f)};  // two independent partial sums
 #pragma unroll
@@ -138,9 +153,9 @@ __device__ __forceinline__ void exp64(const uint32_t (&va)[32], const uint32_t (
       } else {
         x[k] = ffma2(sc, mul2, neg_m);
       }
-      if (MASKED) {
-        x[k].x = (c + e >= lo_c && c + e < hi_c) ? x[k].x : ninf;
-        x[k].y = (c + e + 1 >= lo_c && c + e + 1 < hi_c) ? x[k].y : ninf;
+      if (MASK != kMaskNone) {
+        x[k].x = col_visible<MASK>(c + e, lo_c, hi_c, span) ? x[k].x : ninf;
+        x[k].y = col_visible<MASK>(c + e + 1, lo_c, hi_c, span) ? x[k].y : ninf;
       }
     }
 #pragma unroll
@@ -458,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lo_c = max(J * BN, row_lo) - base;  // visible columns [lo_c, hi_c)
         const int hi_c = min((J + 1) * BN, row_hi) - base;
         const bool masked = !__all_sync(0xffffffffu, lo_c <= 0 && hi_c >= BN);
+        const bool hi_only = __all_sync(0xffffffffu, lo_c <= 0);
         // Pass 1: extreme raw score over the visible columns.  The score
         // transform (scale, then optional softcap) is monotone -- increasing
         // for scale > 0, decreasing for scale < 0 -- so the row max of the
@@ -469,8 +485,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(t_lane + col_s + c, va);
           tmem_ld32(t_lane + col_s + c + 32, vb);
           tmem_wait_ld();
-          ext = masked ? extreme64<UP, true>(va, vb, c, lo_c, hi_c, ext)
-                       : extreme64<UP, false>(va, vb, c, lo_c, hi_c, ext);
+          ext = !masked ? extreme64<UP, kMaskNone>(va, vb, c, lo_c, hi_c, ext)
+                : hi_only ? extreme64<UP, kMaskHi>(va, vb, c, lo_c, hi_c, ext)
+                          : extreme64<UP, kMaskBoth>(va, vb, c, lo_c, hi_c, ext);
         }
         const float mt = (ext == NEG_INF || ext == -NEG_INF)
                              ? NEG_INF
@@ -508,10 +525,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(t_lane + col_s + c + 32, vb);
           tmem_wait_ld();
           uint32_t pw[32];
-          if (masked)
-            exp64<T, CAP, true>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_eff, rs, pw);
+          if (!masked)
+            exp64<T, CAP, kMaskNone>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_eff, rs, pw);
+          else if (hi_only)
+            exp64<T, CAP, kMaskHi>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_eff, rs, pw);
           else
-            exp64<T, CAP, false>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_eff, rs, pw);
+            exp64<T, CAP, kMaskBoth>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_eff, rs, pw);
           tmem_st32(t_lane + col_s + (c >> 1), pw);
           tmem_wait_st();
           tc_fence_before();
