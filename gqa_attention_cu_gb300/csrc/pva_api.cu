@@ -294,7 +294,8 @@ int pva_forward_local(const void* q, const void* k, const void* v, const int32_t
     if ((rc = encode_map(&tq, q, dtype, head_size, num_heads, 64, G, m, true)) != PVA_OK ||
         (rc = encode_map(&tk, k, dtype, head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK ||
         (rc = encode_map(&tv, v, dtype, v_head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK ||
-        (rc = encode_map(&to, o, dtype, v_head_size, num_heads, 64, G, m, true)) != PVA_OK)
+        (rc = encode_map(&to, o, dtype, v_head_size, num_heads, 64, G, out_box_tokens(G),
+                         true)) != PVA_OK)
       return rc;
     if (plan.decode) {
       const int tkeys = decode_tile_keys(head_size);

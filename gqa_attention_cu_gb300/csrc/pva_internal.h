@@ -33,6 +33,9 @@ __host__ __device__ constexpr bool tc_paired(int d, int dv) { return d == dv && 
 __host__ __device__ constexpr int tc_tiles_per_item(int d, int dv) { return tc_paired(d, dv) ? 2 : 1; }
 // Keys per tensor-core key/value tile.
 __host__ __device__ constexpr int tc_block_n(int d, int dv) { return tc_paired(d, dv) ? 128 : 64; }
+// Tokens per TMA store box of the paired kernel's output: one warp's 32 rows
+// (32 / G tokens x G heads) when G divides 32, else the whole 128-row tile.
+__host__ __device__ constexpr int out_box_tokens(int G) { return 32 % G == 0 ? 32 / G : kTcRows / G; }
 // Keys per decode key/value tile for head size D (16 KB of K per tile).
 __host__ __device__ constexpr int decode_tile_keys(int D) { return 8192 / D; }
 

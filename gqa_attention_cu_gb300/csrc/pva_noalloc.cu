@@ -142,7 +142,8 @@ extern "C" int pva_forward_noalloc(const void* q, const void* k, const void* v,
     if ((rc = encode_map(&tq, qa, dtype, head_size, num_heads, 64, G, m, true)) != PVA_OK ||
         (rc = encode_map(&tk, ka, dtype, head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK ||
         (rc = encode_map(&tv, va, dtype, v_head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK ||
-        (rc = encode_map(&to, oa, dtype, v_head_size, num_heads, 64, G, m, true)) != PVA_OK)
+        (rc = encode_map(&to, oa, dtype, v_head_size, num_heads, 64, G, out_box_tokens(G),
+                         true)) != PVA_OK)
       return rc;
     if (plan.decode) {
       const int tkeys = decode_tile_keys(head_size);

@@ -556,44 +556,83 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool whole = tok0 >= own_lo && tok0 + m_tok <= own_hi;
       uint8_t* stage = smem + C::OFF_STAGE + tq * C::STAGE;
       const bool issuer = r == 0;  // lane 0 of the warp with lane quarter 0
+      // G dividing 32: each warp's rows are whole tokens and go out on their own.
+      const bool per_warp = 32 % G == 0;
+      const int tok_w = tok0 + quarter * (32 / G);
+      const bool warp_whole = tok_w >= own_lo && tok_w + 32 / G <= own_hi;
+      // 32 columns at a time; a TMA store leaves per 64-column half.
 #pragma unroll 1
-      for (int c = 0; c < D; c += 64) {
-        uint32_t w[32];  // the row's 64 values of columns [c, c + 64), packed
-#pragma unroll
-        for (int hh = 0; hh < 64; hh += 32) {
+      for (int c = 0; c < D; c += 32) {
+        const bool first = (c & 63) == 0, second = !first;  // position within the half
+        const int unit0 = second ? 4 : 0;                    // 16-byte units of the 128-byte row
+        uint32_t w[16];  // the row's 32 values of columns [c, c + 32), packed
+        {
           uint32_t v[32];
-          tmem_ld32(t_lane + col_o + c + hh, v);
+          tmem_ld32(t_lane + col_o + c, v);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; e += 2)
-            w[(hh + e) >> 1] = pack2<T>(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
+            w[e >> 1] = pack2<T>(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
         }
-        if (whole) {
-          // The staging buffer is free once the previous store has read it.
-          if (issuer) {
-            bulk_wait_read_all();
-            mbar_arrive(&bars->stage_free[tq]);
+        if (per_warp) {
+          // This warp's 32 rows (32 / G whole tokens) leave in their own
+          // 4 KB box: no barrier across the warpgroup.  Lane 0 first waits
+          // until its previous store has read the region.
+          if (warp_whole) {
+            uint8_t* region = stage + quarter * (32 * 128);
+            if (first) {
+              if (lane == 0) bulk_wait_read_all();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(region + lane * 128 + (((unit0 + u) ^ (lane & 7)) << 4)) =
+                  make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+            if (second) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(&tmap_o, region, c - 32, it.unit * G, tok_w);
+                bulk_commit();
+              }
+            }
+          } else if (own) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(out + orow + c + 8 * u) =
+                  make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
           }
-          ok = __all_sync(0xffffffffu, mbar_wait(&bars->stage_free[tq], stages & 1, abort, status));
-          if (!ok) break;
+        } else if (whole) {
+          if (first) {
+            // The staging buffer is free once the previous store has read it.
+            if (issuer) {
+              bulk_wait_read_all();
+              mbar_arrive(&bars->stage_free[tq]);
+            }
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&bars->stage_free[tq], stages & 1, abort, status));
+            if (!ok) break;
+          }
           // Row r: 128 bytes in the 128-byte swizzled layout of the TMA box.
           if (r < G * m_tok) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              *reinterpret_cast<uint4*>(stage + r * 128 + ((u ^ (r & 7)) << 4)) =
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(stage + r * 128 + (((unit0 + u) ^ (r & 7)) << 4)) =
                   make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
           }
-          fence_proxy_async_smem();
-          mbar_arrive(&bars->stage_full[tq]);
-          if (issuer) {
-            if (!(ok = mbar_wait(&bars->stage_full[tq], stages & 1, abort, status))) break;
-            tma_store_3d(&tmap_o, stage, c, it.unit * G, tok0);
-            bulk_commit();
+          if (second) {
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->stage_full[tq]);
+            if (issuer) {
+              if (!(ok = mbar_wait(&bars->stage_full[tq], stages & 1, abort, status))) break;
+              tma_store_3d(&tmap_o, stage, c - 32, it.unit * G, tok0);
+              bulk_commit();
+            }
+            ++stages;
           }
-          ++stages;
         } else if (own) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
+          for (int u = 0; u < 4; ++u)
             *reinterpret_cast<uint4*>(out + orow + c + 8 * u) =
                 make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
@@ -604,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tiles += n;
     }
     // Output stores must be complete before the CTA's shared memory goes.
-    if (r == 0) bulk_wait_all();
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
