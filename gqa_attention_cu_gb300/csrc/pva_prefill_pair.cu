@@ -96,7 +96,7 @@ __device__ __forceinline__ float col_val(const uint32_t (&va)[32], const uint32_
 // of the warp starts inside the tile) and kMaskBoth (lo_c <= col < hi_c, one
 // unsigned compare).  The column is a compile-time constant in the unrolled
 // loops, so a test is one integer compare and one select.
-constexpr int kMaskNone = 0, kMaskHi = 1, kMaskBoth = 2;
+constexpr int kMaskNone = 0, kMaskHi = 1, kMaskBoth = 2, kHalfEmpty = 3;
 template <int MASK>
 __device__ __forceinline__ bool col_visible(int col, int lo_c, int hi_c, unsigned span) {
   if (MASK == kMaskNone) return true;
@@ -472,8 +472,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int base = k0 - it.kv_start;  // local key index of column 0
         const int lo_c = max(J * BN, row_lo) - base;  // visible columns [lo_c, hi_c)
         const int hi_c = min((J + 1) * BN, row_hi) - base;
-        const bool masked = !__all_sync(0xffffffffu, lo_c <= 0 && hi_c >= BN);
-        const bool hi_only = __all_sync(0xffffffffu, lo_c <= 0);
+        // Per 64-column half, decided once for the warp: every column visible,
+        // a one-sided mask (no row starts inside the half), a two-sided mask,
+        // or nothing visible (the half is skipped: P = 0, no exponentials).
+        int mode[BN / 64];
+#pragma unroll
+        for (int c = 0; c < BN; c += 64) {
+          mode[c / 64] = __all_sync(0xffffffffu, lo_c <= c && hi_c >= c + 64) ? kMaskNone
+                         : __all_sync(0xffffffffu, hi_c <= c || lo_c >= c + 64 || hi_c <= lo_c)
+                             ? kHalfEmpty
+                         : __all_sync(0xffffffffu, lo_c <= c) ? kMaskHi
+                                                               : kMaskBoth;
+        }
         // Pass 1: extreme raw score over the visible columns.  The score
         // transform (scale, then optional softcap) is monotone -- increasing
         // for scale > 0, decreasing for scale < 0 -- so the row max of the
@@ -481,13 +491,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         float ext = UP ? NEG_INF : -NEG_INF;
 #pragma unroll
         for (int c = 0; c < BN; c += 64) {
+          const int md = mode[c / 64];
+          if (md == kHalfEmpty) continue;
           uint32_t va[32], vb[32];
           tmem_ld32(t_lane + col_s + c, va);
           tmem_ld32(t_lane + col_s + c + 32, vb);
           tmem_wait_ld();
-          ext = !masked ? extreme64<UP, kMaskNone>(va, vb, c, lo_c, hi_c, ext)
-                : hi_only ? extreme64<UP, kMaskHi>(va, vb, c, lo_c, hi_c, ext)
-                          : extreme64<UP, kMaskBoth>(va, vb, c, lo_c, hi_c, ext);
+          ext = md == kMaskNone ? extreme64<UP, kMaskNone>(va, vb, c, lo_c, hi_c, ext)
+                : md == kMaskHi ? extreme64<UP, kMaskHi>(va, vb, c, lo_c, hi_c, ext)
+                                : extreme64<UP, kMaskBoth>(va, vb, c, lo_c, hi_c, ext);
         }
         const float mt = (ext == NEG_INF || ext == -NEG_INF)
                              ? NEG_INF
@@ -520,17 +532,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 rs = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int c = 0; c < BN; c += 64) {
-          uint32_t va[32], vb[32];
-          tmem_ld32(t_lane + col_s + c, va);
-          tmem_ld32(t_lane + col_s + c + 32, vb);
-          tmem_wait_ld();
+          const int md = mode[c / 64];
           uint32_t pw[32];
-          if (!masked)
-            exp64<T, CAP, kMaskNone>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_eff, rs, pw);
-          else if (hi_only)
-            exp64<T, CAP, kMaskHi>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_eff, rs, pw);
-          else
-            exp64<T, CAP, kMaskBoth>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_eff, rs, pw);
+          if (md == kHalfEmpty) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) pw[e] = 0u;
+          } else {
+            uint32_t va[32], vb[32];
+            tmem_ld32(t_lane + col_s + c, va);
+            tmem_ld32(t_lane + col_s + c + 32, vb);
+            tmem_wait_ld();
+            if (md == kMaskNone)
+              exp64<T, CAP, kMaskNone>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_eff, rs, pw);
+            else if (md == kMaskHi)
+              exp64<T, CAP, kMaskHi>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_eff, rs, pw);
+            else
+              exp64<T, CAP, kMaskBoth>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_eff, rs, pw);
+          }
           tmem_st32(t_lane + col_s + (c >> 1), pw);
           tmem_wait_st();
           tc_fence_before();
