@@ -15,7 +15,7 @@ import threading
 
 from . import workloads  # noqa: F401  (seeded synthetic inputs)
 
-__all__ = ["pva_forward", "pva_forward_local", "pva_get_status", "pva_schedule", "pva_status_string",
+__all__ = ["pva_forward", "pva_forward_local", "pva_forward_padded", "pva_get_status", "pva_schedule", "pva_status_string",
            "pva_last_error", "pva_release", "pva_version", "pva_profile", "pva_kernel_times",
            "pva_selftest_wait", "load_library", "build", "PvaError", "DTYPE_CODES", "DEV_FLAGS"]
 
@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(_PKG, "libpva.so")
 PVA_OK, PVA_ERR_INVALID_ARG, PVA_ERR_UNSUPPORTED, PVA_ERR_CUDA, PVA_ERR_OOM = 0, -1, -2, -3, -4
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
 DEV_FLAGS = {"cu_q_start": 0x1, "cu_kv_start": 0x2, "cu_q_order": 0x4, "cu_kv_order": 0x8,
-             "too_many": 0x10, "null_tensor": 0x20, "wait_timeout": 0x100}
+             "too_many": 0x10, "null_tensor": 0x20, "kv_len": 0x40, "wait_timeout": 0x100}
 
 _lock = threading.Lock()
 _lib = None
@@ -60,6 +60,9 @@ def load_library(path: str | None = None):
         lib.pva_forward_local.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, f, i, i,
                                           vp]
         lib.pva_forward_local.restype = i
+        lib.pva_forward_padded.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, f, i,
+                                           vp]
+        lib.pva_forward_padded.restype = i
         lib.pva_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.pva_get_status.restype = i
         lib.pva_schedule.argtypes = [vp, vp, i, i, i, i, i, i, i,
@@ -138,6 +141,24 @@ def pva_forward_local(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B: int, num_hea
                                int(B), int(num_heads), int(kv_num_heads), int(head_size),
                                int(v_head_size), float(scale), int(is_causal), float(softcap),
                                int(local_window), code, _stream_ptr(stream))
+    _check(rc)
+
+
+def pva_forward_padded(q, k, v, nonpad_kv_seqlen, out, B: int, q_seq: int, kv_seq: int,
+                       num_heads: int, kv_num_heads: int, head_size: int, v_head_size: int,
+                       scale: float = 0.0, is_causal: int = 0, softcap: float = 0.0,
+                       dtype: int | None = None, stream=None) -> None:
+    """The padded form: q [B, q_seq, H, d], k/v [B, kv_seq, Hkv, d/dv], out
+    [B, q_seq, H, dv]; batch entry b's keys are the first
+    ``nonpad_kv_seqlen[b]`` (CUDA int64 [B]) rows of its slot, and the causal
+    limit of query row i is i + nonpad_kv_seqlen[b] - q_seq."""
+    lib = load_library()
+    code = _dtype_code(q) if dtype is None else int(dtype)
+    rc = lib.pva_forward_padded(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                nonpad_kv_seqlen.data_ptr(), out.data_ptr(), int(B), int(q_seq),
+                                int(kv_seq), int(num_heads), int(kv_num_heads), int(head_size),
+                                int(v_head_size), float(scale), int(is_causal), float(softcap),
+                                code, _stream_ptr(stream))
     _check(rc)
 
 

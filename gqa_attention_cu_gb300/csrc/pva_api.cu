@@ -16,6 +16,8 @@
 #include <string>
 #include <utility>
 
+#include <climits>
+
 #include "pva_internal.h"
 
 using namespace pva;
@@ -211,10 +213,12 @@ int get_workspace(int dev, cudaStream_t stream, size_t need, Workspace** out) {
 int prepare(const void* q, const void* k, const void* v, const int32_t* cu_q,
             const int32_t* cu_kv, void* out, int B, int H, int Hkv, int d, int dv, float scale,
             int is_causal, float softcap, int dtype, cudaStream_t stream, Plan* plan,
-            AttnParams* p, int* num_sms) {
+            AttnParams* p, int* num_sms, size_t extra_int_words = 0) {
   int rc = check_and_plan(q, k, v, cu_q, cu_kv, out, B, H, Hkv, d, dv, scale, softcap, dtype,
                           plan);
   if (rc != PVA_OK) return rc;
+  // room after the work lists for offsets the library builds itself
+  plan->int_bytes += (extra_int_words * 4 + 255) / 256 * 256;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -252,33 +256,32 @@ int prepare(const void* q, const void* k, const void* v, const int32_t* cu_q,
   return PVA_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int pva_forward(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
-                const int32_t* cu_seqlens_kv, void* out, int B, int num_heads, int kv_num_heads,
-                int head_size, int v_head_size, float scale, int is_causal, float softcap,
-                int dtype, void* stream_) {
-  return pva_forward_local(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B, num_heads,
-                           kv_num_heads, head_size, v_head_size, scale, is_causal, softcap, 0,
-                           dtype, stream_);
-}
-
-int pva_forward_local(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
-                      const int32_t* cu_seqlens_kv, void* out, int B, int num_heads,
-                      int kv_num_heads, int head_size, int v_head_size, float scale,
-                      int is_causal, float softcap, int local_window, int dtype, void* stream_) {
+// Body shared by the entry points.  `nonpad` (padded layout, device int64 [B])
+// selects the padded form: the offsets and key lengths are then built on the
+// device from q_seq, kv_seq and nonpad, and cu_seqlens_q/kv are ignored.
+int forward_impl(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                 const int32_t* cu_seqlens_kv, void* out, int B, int num_heads,
+                 int kv_num_heads, int head_size, int v_head_size, float scale, int is_causal,
+                 float softcap, int local_window, int dtype, void* stream_,
+                 const int64_t* nonpad, int q_seq, int kv_seq) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   std::lock_guard<std::mutex> lock(g_mu);
   Plan plan;
   AttnParams p{};
   int num_sms = 0;
+  const size_t front_words = nonpad ? 3 * (size_t)(B > 0 ? B : 0) + 2 : 0;
   int rc = prepare(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B, num_heads, kv_num_heads,
                    head_size, v_head_size, scale, is_causal, softcap, dtype, stream, &plan, &p,
-                   &num_sms);
+                   &num_sms, front_words);
   if (rc != PVA_OK) return rc;
   p.window = local_window > 0 ? local_window : 0;
+  int32_t* front = nullptr;
+  if (nonpad) {
+    front = p.ws + WsLayout{B, kv_num_heads}.int_words();
+    p.cu_q = front;
+    p.cu_kv = front + B + 1;
+    p.kv_len = front + 2 * B + 2;
+  }
 
   CUtensorMap tq, tk, tv, to, dk, dvm;
   if (plan.tensor_core) {
@@ -314,7 +317,13 @@ int pva_forward_local(const void* q, const void* k, const void* v, const int32_t
     cudaGetDevice(&g_prof.dev);
   }
   prof_mark(0, stream);
-  cudaError_t e = launch_scheduler(p, plan.sched, stream);
+  cudaError_t e = cudaSuccess;
+  if (nonpad) {
+    e = launch_padded_front(nonpad, B, q_seq, kv_seq, front, front + B + 1, front + 2 * B + 2,
+                            stream);
+    if (e != cudaSuccess) return cuda_fail(e, "padded front-end launch");
+  }
+  e = launch_scheduler(p, plan.sched, stream);
   if (e != cudaSuccess) return cuda_fail(e, "scheduler launch");
   prof_mark(1, stream);
   if (!plan.tensor_core) {
@@ -334,6 +343,46 @@ int pva_forward_local(const void* q, const void* k, const void* v, const int32_t
     prof_mark(3, stream);
   }
   return PVA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pva_forward(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                const int32_t* cu_seqlens_kv, void* out, int B, int num_heads, int kv_num_heads,
+                int head_size, int v_head_size, float scale, int is_causal, float softcap,
+                int dtype, void* stream) {
+  return forward_impl(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B, num_heads, kv_num_heads,
+                      head_size, v_head_size, scale, is_causal, softcap, 0, dtype, stream,
+                      nullptr, 0, 0);
+}
+
+int pva_forward_local(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                      const int32_t* cu_seqlens_kv, void* out, int B, int num_heads,
+                      int kv_num_heads, int head_size, int v_head_size, float scale,
+                      int is_causal, float softcap, int local_window, int dtype, void* stream) {
+  return forward_impl(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B, num_heads, kv_num_heads,
+                      head_size, v_head_size, scale, is_causal, softcap, local_window, dtype,
+                      stream, nullptr, 0, 0);
+}
+
+int pva_forward_padded(const void* q, const void* k, const void* v,
+                       const int64_t* nonpad_kv_seqlen, void* out, int B, int q_seq, int kv_seq,
+                       int num_heads, int kv_num_heads, int head_size, int v_head_size,
+                       float scale, int is_causal, float softcap, int dtype, void* stream) {
+  if (!nonpad_kv_seqlen) return fail(PVA_ERR_INVALID_ARG, "null nonpad_kv_seqlen pointer");
+  if (B < 1) return fail(PVA_ERR_INVALID_ARG, "B must be >= 1");
+  if (q_seq < 0 || kv_seq < 0)
+    return fail(PVA_ERR_INVALID_ARG, "q_seq and kv_seq must be non-negative");
+  if ((long long)B * q_seq > INT_MAX || (long long)B * kv_seq > INT_MAX)
+    return fail(PVA_ERR_INVALID_ARG, "B * q_seq and B * kv_seq must fit in int32");
+  // The offsets are built on the device; the nonpad pointer stands in for them
+  // in the host checks (which only test that they are non-null).
+  const int32_t* stand_in = reinterpret_cast<const int32_t*>(nonpad_kv_seqlen);
+  return forward_impl(q, k, v, stand_in, stand_in, out, B, num_heads, kv_num_heads, head_size,
+                      v_head_size, scale, is_causal, softcap, 0, dtype, stream,
+                      nonpad_kv_seqlen, q_seq, kv_seq);
 }
 
 int pva_get_status(void* stream_, uint32_t* device_flags) {

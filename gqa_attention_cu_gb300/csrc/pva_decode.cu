@@ -82,7 +82,7 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, const SchedHead
   r.s = local - r.g * r.S;
   r.kv_start = p.cu_kv[r.b];
   r.q_tok = p.cu_q[r.b];
-  const int lkv = p.cu_kv[r.b + 1] - r.kv_start;
+  const int lkv = p.kv_len ? p.kv_len[r.b] : p.cu_kv[r.b + 1] - r.kv_start;
   // A local window W keeps the last W keys (the one query row sits at the end).
   const int kbeg = p.window > 0 && p.window < lkv ? lkv - p.window : 0;
   const int per = (lkv - kbeg + r.S - 1) / r.S;

@@ -84,6 +84,10 @@ struct AttnParams {
   void* out;
   const int32_t* cu_q;
   const int32_t* cu_kv;
+  // Optional [B]: the valid keys of each sequence, which then sits at the
+  // start of its slot [cu_kv[b], cu_kv[b+1]) (padded K/V); nullptr: the whole
+  // slot is the sequence.
+  const int32_t* kv_len;
   int B, H, Hkv, G, d, dv;
   float scale;    // resolved (default already applied)
   float softcap;  // 0 = off
@@ -144,6 +148,8 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size
 
 // ---- launchers (defined next to their kernels) -------------------------------
 cudaError_t launch_scheduler(const AttnParams& p, const SchedConfig& c, cudaStream_t s);
+cudaError_t launch_padded_front(const int64_t* nonpad, int B, int q_seq, int kv_seq,
+                                int32_t* cu_q, int32_t* cu_kv, int32_t* kv_len, cudaStream_t s);
 cudaError_t launch_prefill_f32(const AttnParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_prefill_tc(const AttnParams& p, int dtype, const CUtensorMap& tq,
                               const CUtensorMap& tk, const CUtensorMap& tv, int num_sms,

@@ -37,8 +37,9 @@ __device__ __forceinline__ PrefillItem decode_prefill_item(const AttnParams& p,
   r.b = order[pos];
   r.q_start = p.cu_q[r.b];
   r.kv_start = p.cu_kv[r.b];
+  // (padded K/V: the sequence's keys are the first kv_len[b] of its slot)
   r.lq = p.cu_q[r.b + 1] - r.q_start;
-  r.lkv = p.cu_kv[r.b + 1] - r.kv_start;
+  r.lkv = p.kv_len ? p.kv_len[r.b] : p.cu_kv[r.b + 1] - r.kv_start;
   const int n_tiles = (r.lq + h.tile_tokens - 1) / h.tile_tokens;
   const int rank = local / h.units_per_tile;
   r.unit = local - rank * h.units_per_tile;

@@ -74,11 +74,12 @@ struct SeqLens {
 struct Lengths {
   const int32_t* cu_q;
   const int32_t* cu_kv;
+  const int32_t* kv_len;  // padded K/V lengths, or nullptr
   const int* s_lq;   // nullptr when not staged
   const int* s_lkv;
   __device__ __forceinline__ SeqLens operator()(int b) const {
     if (s_lq) return SeqLens{s_lq[b], s_lkv[b]};
-    return SeqLens{cu_q[b + 1] - cu_q[b], cu_kv[b + 1] - cu_kv[b]};
+    return SeqLens{cu_q[b + 1] - cu_q[b], kv_len ? kv_len[b] : cu_kv[b + 1] - cu_kv[b]};
   }
 };
 
@@ -212,7 +213,8 @@ __global__ void __launch_bounds__(NT) pva_schedule_kernel(AttnParams p, SchedCon
   int32_t* ws = p.ws;
   SchedHeader* hdr = reinterpret_cast<SchedHeader*>(ws + kWsHeader);
   const bool staged = B <= kSortMax;
-  const Lengths seq_lens{p.cu_q, p.cu_kv, staged ? s_lq : nullptr, staged ? s_lkv : nullptr};
+  const Lengths seq_lens{p.cu_q, p.cu_kv, p.kv_len, staged ? s_lq : nullptr,
+                         staged ? s_lkv : nullptr};
 
   if (threadIdx.x == 0) s_status = 0;
   __syncthreads();
@@ -228,9 +230,11 @@ __global__ void __launch_bounds__(NT) pva_schedule_kernel(AttnParams p, SchedCon
   }
   for (int b = threadIdx.x; b < B; b += NT) {
     const int lq = p.cu_q[b + 1] - p.cu_q[b];
-    const int lkv = p.cu_kv[b + 1] - p.cu_kv[b];
+    const int slot = p.cu_kv[b + 1] - p.cu_kv[b];
+    const int lkv = p.kv_len ? p.kv_len[b] : slot;
     if (lq < 0) atomicOr(&s_status, PVA_DEV_CU_Q_ORDER);
-    if (lkv < 0) atomicOr(&s_status, PVA_DEV_CU_KV_ORDER);
+    if (slot < 0) atomicOr(&s_status, PVA_DEV_CU_KV_ORDER);
+    if (lkv < 0 || lkv > slot) atomicOr(&s_status, PVA_DEV_KV_LEN);
     if (staged) {
       s_lq[b] = lq;
       s_lkv[b] = lkv;
@@ -313,6 +317,33 @@ __global__ void __launch_bounds__(NT) pva_schedule_kernel(AttnParams p, SchedCon
 }
 
 }  // namespace
+
+// Front end of pva_forward_padded: the padded layout as packed offsets.  Batch
+// b's queries are rows [b q_seq, (b+1) q_seq) and its key/value slot rows
+// [b kv_seq, (b+1) kv_seq), of which the first nonpad[b] are its keys (the
+// exclusive prefix sum of the pages' nonpad_kv_seqlen, taken over slots
+// instead of over packed keys, so nothing is copied).  A length outside
+// [0, kv_seq] is stored as -1, which the scheduler reports as PVA_DEV_KV_LEN.
+__global__ void pva_padded_front_kernel(const int64_t* nonpad, int B, int q_seq, int kv_seq,
+                                        int32_t* cu_q, int32_t* cu_kv, int32_t* kv_len) {
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b <= B; b += gridDim.x * blockDim.x) {
+    cu_q[b] = b * q_seq;
+    cu_kv[b] = b * kv_seq;
+    if (b < B) {
+      const long long n = nonpad[b];
+      kv_len[b] = (n < 0 || n > kv_seq) ? -1 : (int32_t)n;
+    }
+  }
+}
+
+cudaError_t launch_padded_front(const int64_t* nonpad, int B, int q_seq, int kv_seq,
+                                int32_t* cu_q, int32_t* cu_kv, int32_t* kv_len, cudaStream_t s) {
+  const int threads = 256, blocks = (B + threads) / threads;
+  pva_padded_front_kernel<<<blocks < 1024 ? blocks : 1024, threads, 0, s>>>(nonpad, B, q_seq,
+                                                                          kv_seq, cu_q, cu_kv,
+                                                                          kv_len);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_scheduler(const AttnParams& p, const SchedConfig& c, cudaStream_t s) {
   if (p.B <= 128)

@@ -56,6 +56,7 @@ typedef enum { PVA_F32 = 0, PVA_F16 = 1, PVA_BF16 = 2 } pva_dtype;
 #define PVA_DEV_CU_KV_ORDER 0x8u  /* cu_seqlens_kv decreases somewhere */
 #define PVA_DEV_TOO_MANY 0x10u    /* work count does not fit the 32-bit work index */
 #define PVA_DEV_NULL_TENSOR 0x20u /* a NULL q/k/v/out with a nonzero token extent */
+#define PVA_DEV_KV_LEN 0x40u      /* pva_forward_padded: a nonpad length outside [0, kv_seq] */
 #define PVA_DEV_WAIT_TIMEOUT 0x100u /* a pipeline wait in a kernel gave up (never expected) */
 
 /*
@@ -120,6 +121,39 @@ int pva_forward_local(const void* q, const void* k, const void* v,
                       void* out, int B, int num_heads, int kv_num_heads,
                       int head_size, int v_head_size, float scale, int is_causal,
                       float softcap, int local_window, int dtype, void* stream);
+
+/*
+ * pva_forward_padded -- the padded form of the same attention: the opset-24
+ * Attention input `nonpad_kv_seqlen` of the packed_varlen_attention.rs module
+ * doc ("Relationship to ONNX Attention-24 nonpad_kv_seqlen") and of the
+ * attention.rs page (the per-batch causal offset and padding frontier built
+ * before the launch).  Batch entry b has q_seq query rows and a key/value slot
+ * of kv_seq rows, of which the first nonpad_kv_seqlen[b] are its keys; query
+ * row i sees key j iff j < nonpad_kv_seqlen[b] and, when is_causal,
+ * j <= i + nonpad_kv_seqlen[b] - q_seq.  That is exactly pva_forward on the
+ * same rows with the padding removed (cu_seqlens_kv the exclusive prefix sum
+ * of nonpad_kv_seqlen); here nothing is copied or repacked.
+ *
+ * q    : [B, q_seq, num_heads, head_size]      (every query row is real)
+ * k    : [B, kv_seq, kv_num_heads, head_size]
+ * v    : [B, kv_seq, kv_num_heads, v_head_size]
+ * out  : [B, q_seq, num_heads, v_head_size]    (every row written)
+ * nonpad_kv_seqlen : device pointer to int64 [B].  A value outside
+ *        [0, kv_seq] latches PVA_DEV_KV_LEN on the device; nothing is computed
+ *        and `out` is left untouched.
+ * B >= 1, q_seq >= 0, kv_seq >= 0, and B * q_seq and B * kv_seq must fit in
+ * int32 (else PVA_ERR_INVALID_ARG, nothing enqueued).  The padding rows of k
+ * and v are never attended, but they must hold finite values: a key tile that
+ * reaches into them multiplies them by zero weights on the tensor cores, and
+ * 0 * NaN or 0 * inf is NaN.  The offsets are built on the device by a small
+ * kernel in the stream, inside the library's workspace.  Other arguments,
+ * errors, memory and asynchrony: as pva_forward.
+ */
+int pva_forward_padded(const void* q, const void* k, const void* v,
+                       const int64_t* nonpad_kv_seqlen, void* out, int B, int q_seq,
+                       int kv_seq, int num_heads, int kv_num_heads, int head_size,
+                       int v_head_size, float scale, int is_causal, float softcap,
+                       int dtype, void* stream);
 
 /*
  * pva_forward_noalloc -- the same attention as pva_forward, for callers that

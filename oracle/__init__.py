@@ -11,6 +11,8 @@ double-precision loop nest (see its header for the passages of the
 doc sections "Packed layout & cumulative offsets", "Schema (v1)", "Causal
 alignment", and the five kernel stages).  This module only compiles it with
 gcc, marshals numpy arrays, and widens bf16/f16/f32 inputs to float64 (exact).
+``attention_padded`` is the padded form of the opset-24 ``nonpad_kv_seqlen``
+input (attention.rs), written separately over the padded layout.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (library cross-checks, closed forms, invariants, hand-derived golden values).
@@ -68,6 +70,9 @@ def _bind(path: str):
     lib.pva_oracle_rows_window.argtypes = [dp, dp, dp, ip, ip, lp, ctypes.c_int64, dp,
                                            i, i, i, i, i, d, i, d, i, i]
     lib.pva_oracle_rows_window.restype = i
+    lib.pva_oracle_forward_padded.argtypes = [dp, dp, dp, lp, dp, i, i, i, i, i, i, i, d, i, d,
+                                              i]
+    lib.pva_oracle_forward_padded.restype = i
     lib.pva_oracle_max_threads.argtypes = []
     lib.pva_oracle_max_threads.restype = i
     return lib
@@ -128,6 +133,32 @@ def resolve_scale(scale: float, head_size: int) -> float:
     if scale != 0.0:
         return float(np.float32(scale))
     return float(np.float32(1.0) / np.sqrt(np.float32(head_size)))
+
+
+def attention_padded(q, k, v, nonpad_kv_seqlen, num_heads: int, kv_num_heads: int,
+                     scale: float = 0.0, is_causal: bool = False, softcap: float = 0.0,
+                     threads: int = 0) -> np.ndarray:
+    """fp64 attention in the padded layout of the opset-24 ``nonpad_kv_seqlen``
+    input: q [B, q_seq, H, d], k [B, kv_seq, Hkv, d], v [B, kv_seq, Hkv, dv],
+    nonpad int [B].  Returns float64 [B, q_seq, H, dv]."""
+    lib = _load()
+    qd, kd, vd = _as_f64(q), _as_f64(k), _as_f64(v)
+    npd = nonpad_kv_seqlen
+    if hasattr(npd, "detach"):
+        npd = npd.detach().to("cpu").numpy()
+    npd = np.ascontiguousarray(np.asarray(npd, dtype=np.int64))
+    B, q_seq, H, d = qd.shape
+    kv_seq, Hkv, dv = kd.shape[1], kd.shape[2], vd.shape[3]
+    if H != int(num_heads) or Hkv != int(kv_num_heads) or npd.shape != (B,):
+        raise ValueError("shapes do not match the head counts / batch")
+    out = np.zeros((B, q_seq, H, dv), dtype=np.float64)
+    rc = lib.pva_oracle_forward_padded(
+        _ptr(qd, ctypes.c_double), _ptr(kd, ctypes.c_double), _ptr(vd, ctypes.c_double),
+        _ptr(npd, ctypes.c_int64), _ptr(out, ctypes.c_double), B, q_seq, kv_seq, H, Hkv, d, dv,
+        resolve_scale(scale, d), int(bool(is_causal)), float(np.float32(softcap)), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return out
 
 
 def max_threads() -> int:

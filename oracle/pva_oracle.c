@@ -229,6 +229,85 @@ int pva_oracle_rows(const double* q, const double* k, const double* v,
                                 dv, scale, is_causal, softcap, 0, nthreads);
 }
 
+/* Padded form: the opset-24 Attention input `nonpad_kv_seqlen` (attention.rs,
+ * the per-batch causal offset and padding frontier set up before the launch;
+ * packed_varlen_attention.rs, module doc "Relationship to ONNX Attention-24
+ * nonpad_kv_seqlen").  Batch entry b has q_seq query rows and a slot of kv_seq
+ * key/value rows: q [B, q_seq, H, d], k [B, kv_seq, Hkv, d],
+ * v [B, kv_seq, Hkv, dv], out [B, q_seq, H, dv].  Query row i of entry b sees
+ * slot row j iff j < nonpad[b] (the padding frontier, in every mode) and, when
+ * causal, j <= i + offset with offset = nonpad[b] - q_seq.  Written on its own
+ * over the padded layout (no packing), so that the tests can hold it against
+ * the packed definition above. */
+int pva_oracle_forward_padded(const double* q, const double* k, const double* v,
+                              const int64_t* nonpad, double* out, int B, int q_seq, int kv_seq,
+                              int H, int Hkv, int d, int dv, double scale, int is_causal,
+                              double softcap, int nthreads) {
+  if (!nonpad || B < 1 || q_seq < 0 || kv_seq < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 ||
+      d <= 0 || dv <= 0)
+    return ORACLE_BAD_ARG;
+  for (int b = 0; b < B; ++b)
+    if (nonpad[b] < 0 || nonpad[b] > kv_seq) return ORACLE_BAD_ARG;
+  const int group = H / Hkv;
+  const int64_t n_rows = (int64_t)B * q_seq * H;
+  int failed = 0;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+#pragma omp parallel
+  {
+    double* w = (double*)malloc(sizeof(double) * (size_t)(kv_seq > 0 ? kv_seq : 1));
+    if (!w) {
+#pragma omp atomic write
+      failed = 1;
+    }
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t row = 0; row < n_rows; ++row) {
+      if (!w) continue;
+      const int h = (int)(row % H);
+      const int64_t bi = row / H;               /* b * q_seq + i */
+      const int b = (int)(bi / q_seq);
+      const int64_t i = bi % q_seq;
+      const int g = h / group;
+      const int64_t limit = nonpad[b];           /* padding frontier */
+      const int64_t offset = nonpad[b] - q_seq;  /* causal offset */
+      const double* qrow = q + row * (int64_t)d;
+      double* orow = out + row * (int64_t)dv;
+      double m = -INFINITY;
+      int any = 0;
+      for (int64_t j = 0; j < kv_seq; ++j) {
+        const int visible = j < limit && (!is_causal || j <= i + offset);
+        w[j] = -INFINITY;
+        if (!visible) continue;
+        const double* krow = k + (((int64_t)b * kv_seq + j) * Hkv + g) * (int64_t)d;
+        double dot = 0.0;
+        for (int p = 0; p < d; ++p) dot += qrow[p] * krow[p];
+        double s = scale * dot;
+        if (softcap != 0.0) s = softcap * tanh(s / softcap);
+        w[j] = s;
+        if (s > m) m = s;
+        any = 1;
+      }
+      for (int c = 0; c < dv; ++c) orow[c] = 0.0;
+      if (!any) continue;
+      double l = 0.0;
+      for (int64_t j = 0; j < kv_seq; ++j) {
+        w[j] = w[j] == -INFINITY ? 0.0 : exp(w[j] - m);
+        l += w[j];
+      }
+      for (int64_t j = 0; j < kv_seq; ++j) {
+        if (w[j] == 0.0) continue;
+        const double* vrow = v + (((int64_t)b * kv_seq + j) * Hkv + g) * (int64_t)dv;
+        for (int c = 0; c < dv; ++c) orow[c] += (w[j] / l) * vrow[c];
+      }
+    }
+    free(w);
+  }
+  return failed ? ORACLE_OOM : ORACLE_OK;
+}
+
 /* Threads OpenMP would use by default (reported with CPU timings). */
 int pva_oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -77,3 +77,26 @@ def test_host_argument_checks_need_no_gpu(lib, kw, code):
 def test_python_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(pva.PvaError):
         pva.load_library(str(tmp_path / "missing.so"))
+
+
+def _call_padded(lib, **kw):
+    args = dict(q=16, k=16, v=16, nonpad=16, out=16, B=2, q_seq=4, kv_seq=8, H=4, Hkv=2, d=128,
+                dv=128, scale=0.0, causal=0, softcap=0.0, dtype=2)
+    args.update(kw)
+    return lib.pva_forward_padded(args["q"], args["k"], args["v"], args["nonpad"], args["out"],
+                                  args["B"], args["q_seq"], args["kv_seq"], args["H"],
+                                  args["Hkv"], args["d"], args["dv"], args["scale"],
+                                  args["causal"], args["softcap"], args["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(nonpad=None), -1), (dict(B=0), -1), (dict(q_seq=-1), -1), (dict(kv_seq=-3), -1),
+    (dict(B=3, q_seq=1 << 30), -1), (dict(B=5, kv_seq=1 << 29), -1),
+    (dict(H=6, Hkv=4), -1), (dict(d=80, dv=80), -2), (dict(dtype=7), -1),
+])
+def test_padded_host_argument_checks_need_no_gpu(lib, kw, code):
+    """pva_forward_padded rejects malformed calls on the host, before any CUDA
+    call (its extra rules: a non-null nonpad_kv_seqlen, non-negative q_seq and
+    kv_seq, B * q_seq and B * kv_seq within int32)."""
+    assert _call_padded(lib, **kw) == code
+    assert pva.pva_last_error() != ""

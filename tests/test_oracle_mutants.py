@@ -40,6 +40,15 @@ MUTANTS = [
     ("window_off_by_one", "j < frontier + 1 - local_window", "j <= frontier + 1 - local_window"),
     ("window_from_row_not_limit", "j < frontier + 1 - local_window", "j < i + 1 - local_window"),
     ("window_ignored", "if (local_window > 0 && j < frontier + 1 - local_window)", "if (0)"),
+    ("padded_frontier_dropped", "const int visible = j < limit &&", "const int visible ="),
+    ("padded_offset_from_slot", "const int64_t offset = nonpad[b] - q_seq;",
+     "const int64_t offset = kv_seq - q_seq;"),
+    ("padded_frontier_inclusive", "const int visible = j < limit &&",
+     "const int visible = j <= limit &&"),
+    ("padded_head_map", "const int g = h / group;\n      const int64_t limit",
+     "const int g = h % Hkv;\n      const int64_t limit"),
+    ("padded_value_batch_stride", "v + (((int64_t)b * kv_seq + j)", "v + (((int64_t)b * q_seq + j)"),
+    ("padded_no_normalise", "orow[c] += (w[j] / l) * vrow[c];", "orow[c] += w[j] * vrow[c];"),
 ]
 
 
@@ -69,6 +78,11 @@ def _pin_checks():
         ("window", lambda: ([pins.test_window_row_is_plain_attention_over_the_window_keys(s, c)
                              for s in range(2) for c in (False, True)],
                             pins.test_window_of_one_returns_the_value_row_at_the_causal_limit())),
+        ("padded", lambda: ([pins.test_padded_form_matches_sdpa_with_both_frontiers(s)
+                             for s in range(6)],
+                            [pins.test_padded_form_equals_packed_form_on_the_prefix_sum(s)
+                             for s in range(6)],
+                            pins.test_padded_form_ignores_what_the_padding_holds())),
         ("closed_forms", lambda: (pins.test_constant_value_rows_return_that_row(),
                                   pins.test_zero_query_gives_mean_of_visible_values(),
                                   pins.test_empty_sequences_and_fully_masked_rows_are_zero())),

@@ -421,3 +421,79 @@ def test_window_rows_api_matches_full_forward():
     rows = np.arange(full.shape[0] * H)[::3]
     got = oracle.attention_rows(q, k, v, cq, ck, rows, H, Hkv, 0.0, True, local_window=3)
     np.testing.assert_array_equal(got, full.reshape(-1, full.shape[-1])[rows])
+
+
+# ---------------------------------------------------------------------------
+# The padded form (opset-24 nonpad_kv_seqlen; attention.rs per-batch causal
+# offset and padding frontier), written separately over the padded layout
+# ---------------------------------------------------------------------------
+def _padded_case(seed, causal=None):
+    g = torch.Generator().manual_seed(700 + seed)
+    B, H, Hkv, d, dv = 4, 6, 2, 8, 5
+    q_seq = int(torch.randint(1, 7, (1,), generator=g))
+    kv_seq = int(torch.randint(1, 12, (1,), generator=g))
+    nonpad = torch.randint(0, kv_seq + 1, (B,), generator=g).tolist()
+    nonpad[0] = kv_seq  # one full slot
+    q = torch.randn(B, q_seq, H, d, generator=g, dtype=torch.float64)
+    k = torch.randn(B, kv_seq, Hkv, d, generator=g, dtype=torch.float64)
+    v = torch.randn(B, kv_seq, Hkv, dv, generator=g, dtype=torch.float64)
+    if causal is None:
+        causal = bool(seed % 2)
+    return q, k, v, nonpad, H, Hkv, causal
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_padded_form_matches_sdpa_with_both_frontiers(seed):
+    """attention_padded against torch float64 SDPA given the padded op's
+    explicit mask: j < nonpad[b], and (causal) j <= i + nonpad[b] - q_seq."""
+    q, k, v, nonpad, H, Hkv, causal = _padded_case(seed)
+    B, q_seq, _, d = q.shape
+    kv_seq = k.shape[1]
+    out = oracle.attention_padded(q, k, v, nonpad, H, Hkv, 0.0, causal, softcap=0.0)
+    i = torch.arange(q_seq).view(-1, 1)
+    j = torch.arange(kv_seq).view(1, -1)
+    for b in range(B):
+        mask = (j < nonpad[b]).expand(q_seq, kv_seq)
+        if causal:
+            mask = mask & (j <= i + (nonpad[b] - q_seq))
+        ref = torch.nan_to_num(_sdpa_seq(q[b], k[b], v[b], oracle.resolve_scale(0.0, d), mask),
+                               nan=0.0)
+        np.testing.assert_allclose(out[b], ref.numpy(), rtol=0, atol=1e-12)
+        assert np.all(out[b][~mask.any(dim=1).numpy()] == 0.0)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_padded_form_equals_packed_form_on_the_prefix_sum(seed):
+    """The two representations the module doc relates: the padded op equals
+    the packed op fed cu_seqlens_kv = exclusive prefix sum of nonpad (its
+    rows packed) and cu_seqlens_q of equal q_seq lengths.  Two separate loop
+    nests, so this holds each against the other; softcap included."""
+    q, k, v, nonpad, H, Hkv, causal = _padded_case(seed)
+    B, q_seq, _, d = q.shape
+    softcap = 0.0 if seed < 3 else 1.5
+    out = oracle.attention_padded(q, k, v, nonpad, H, Hkv, 0.3, causal, softcap)
+    kp = torch.cat([k[b, :nonpad[b]] for b in range(B)])
+    vp = torch.cat([v[b, :nonpad[b]] for b in range(B)])
+    packed = oracle.attention(q.reshape(B * q_seq, H, d), kp, vp,
+                              workloads.cu_from_lengths([q_seq] * B),
+                              workloads.cu_from_lengths(nonpad), H, Hkv, 0.3, causal, softcap)
+    np.testing.assert_allclose(out.reshape(packed.shape), packed, rtol=0, atol=1e-13)
+
+
+def test_padded_form_ignores_what_the_padding_holds():
+    q, k, v, nonpad, H, Hkv, _ = _padded_case(11, causal=True)
+    nonpad[1] = 0
+    a = oracle.attention_padded(q, k, v, nonpad, H, Hkv, 0.0, True)
+    k2, v2 = k.clone(), v.clone()
+    for b, n in enumerate(nonpad):
+        k2[b, n:] = 1e6
+        v2[b, n:] = -7.0
+    np.testing.assert_array_equal(oracle.attention_padded(q, k2, v2, nonpad, H, Hkv, 0.0, True), a)
+    assert np.all(a[1] == 0.0)
+
+
+def test_padded_form_rejects_lengths_outside_the_slot():
+    q, k, v, nonpad, H, Hkv, causal = _padded_case(2)
+    for bad in (-1, k.shape[1] + 1):
+        with pytest.raises(ValueError):
+            oracle.attention_padded(q, k, v, [bad] + nonpad[1:], H, Hkv, 0.0, causal)
