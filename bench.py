@@ -41,6 +41,10 @@ WORKLOAD_TEXT = {
                 "d=192, dv=128, N(0,1)",
     "bf16_window": "bf16 causal GQA prefill with a local window of 4096 keys: B=4, "
                    "L~logU[8192,32768], H=32, Hkv=8, d=dv=128, N(0,1)",
+    "bf16_kvcache_decode": "bf16 GroupQueryAttention decode step on a BNSH KV cache of capacity "
+                           "8192: B=256, keys after the append ~U[512,8192], H=32, Hkv=8, "
+                           "d=128, rotary on 128 dims (half-split, f32 tables), append + "
+                           "rotary + attention",
 }
 METRIC = "varlen attn TFLOP/s (prefill) & KV-read GB/s (decode), % of roofline"
 L2_FLUSH_BYTES = 256 << 20
@@ -257,6 +261,57 @@ class OracleSampler:
         return pairs * 2 * (sp.head_size + sp.v_head_size) / secs / 1e12, "TFLOP/s"
 
 
+class CacheStepSampler:
+    """Times the cache-step oracle (metadata, append, rotary, fp64 attention)
+    on bounded samples: a few sequences of the workload's total-length draw
+    per call, each with its own small cache.  Work is the K/V bytes of the
+    valid cache rows, counted as the GPU arm counts them."""
+
+    def __init__(self, w_name: str, seed: int = 0):
+        import torch
+
+        from gqa_attention_cu_gb300 import workloads
+        self.torch, self.wl, self.name = torch, workloads, w_name
+        self.spec = workloads.WORKLOADS[w_name]
+        # the totals make_cache_step draws for this seed
+        self.totals = torch.randint(self.spec.params["lo"], self.spec.params["hi"] + 1,
+                                    (self.spec.B,),
+                                    generator=torch.Generator("cpu").manual_seed(seed)).tolist()
+        self.gen = torch.Generator("cpu").manual_seed(seed + 11)
+        self.cos, self.sin = workloads.rotary_tables(self.spec.params["cache_rows"],
+                                                     self.spec.params["rotary_dim"])
+        self.next = 0
+
+    def _one(self):
+        from oracle import gqa_cache
+        torch, sp = self.torch, self.spec
+        tot = [self.totals[(self.next + i) % len(self.totals)] for i in range(2)]
+        self.next += 2
+        cap, H, Hkv, d = max(tot), sp.num_heads, sp.kv_num_heads, sp.head_size
+        td = self.wl.DTYPES[sp.dtype]
+        r = lambda *shape: torch.randn(shape, generator=self.gen).to(td)  # noqa: E731
+        q, kn, vn = r(2, 1, H, d), r(2, 1, Hkv, d), r(2, 1, Hkv, d)
+        kc, vc = r(2, Hkv, cap, d), r(2, Hkv, cap, d)
+        t0 = time.perf_counter()
+        gqa_cache.gqa_cache_step(q, kn, vn, kc, vc, [t - 1 for t in tot], H, Hkv, self.cos,
+                                 self.sin)
+        return time.perf_counter() - t0, sum(tot) * Hkv * 2 * d * 2
+
+    def run(self, seconds: float):
+        tot_t = tot_b = n = 0
+        while tot_t < seconds:
+            dt, nb = self._one()
+            tot_t, tot_b, n = tot_t + dt, tot_b + nb, n + 2
+        return tot_t, tot_b, n
+
+    def value(self, secs: float, kv_bytes: int):
+        return kv_bytes / secs / 1e9, "GB/s"
+
+
+def make_sampler(w_name: str):
+    return CacheStepSampler(w_name) if w_name == "bf16_kvcache_decode" else OracleSampler(w_name)
+
+
 def run_reference(args, w_name):
     """The fp64 CPU oracle, timed on the host cores, on a bounded sample of the
     workload per step (rank 0 only; other ranks exit without work)."""
@@ -264,7 +319,7 @@ def run_reference(args, w_name):
     if rank != 0:
         return
     import oracle
-    smp = OracleSampler(w_name)
+    smp = make_sampler(w_name)
     for _ in range(args.warmup):
         smp.run(args.ref_seconds / 4)
     secs = pairs = rows = 0
@@ -273,7 +328,10 @@ def run_reference(args, w_name):
         secs, pairs, rows = secs + t, pairs + p, rows + r
     value, unit = smp.value(secs, pairs)
     sample = (f"~{args.ref_seconds:g} s of oracle work per step: {rows // args.steps} random "
-              f"(token, head) output rows per step from sequences of the workload's length draw")
+              f"(token, head) output rows per step from sequences of the workload's length draw"
+              if w_name != "bf16_kvcache_decode" else
+              f"~{args.ref_seconds:g} s of oracle work per step: {rows // args.steps} sequences "
+              f"of the workload's length draw per step, whole cache step each")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -291,12 +349,136 @@ def run_reference(args, w_name):
 def cpu_baseline(w_name, seconds=12.0):
     """The oracle as it stands on the host cores, on a bounded sample."""
     import oracle
-    smp = OracleSampler(w_name)
+    smp = make_sampler(w_name)
     secs, pairs, rows = smp.run(seconds)
     value, unit = smp.value(secs, pairs)
+    what = ("sequences of the workload's length draw, whole cache step each"
+            if w_name == "bf16_kvcache_decode" else
+            "random (token, head) output rows from sequences of the workload's length draw")
     return {"value": value, "unit": unit, "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"{rows} random (token, head) output rows from sequences of the "
-                      f"workload's length draw, {secs:.1f} s"}
+            "sample": f"{rows} {what}, {secs:.1f} s"}
+
+
+def bench_kvcache(args, rank, world, local, dev):
+    """One GroupQueryAttention decode step per timed step (pva_gqa_kvcache):
+    metadata, append + rotary, scheduler and split-KV decode straight from the
+    BNSH caches.  The step is repeatable: with the same seqlens_k it rewrites
+    the same cache row each time.  Metric: K/V bytes of the valid cache rows
+    per second (each row read once for its kv head's G query heads)."""
+    import torch
+
+    import gqa_attention_cu_gb300 as pva
+    from gqa_attention_cu_gb300 import workloads
+
+    w_name = args.workload
+    c = workloads.make_cache_step(w_name, seed=rank, B=args.batch, device=str(dev))
+    H, Hkv, d = c["num_heads"], c["kv_num_heads"], c["head_size"]
+    kv_bytes = sum(c["totals"]) * Hkv * 2 * d * 2
+    stream = torch.cuda.Stream(device=dev)
+    out = torch.empty_like(c["q"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(q, kn, vn, sk, s):
+        pva.pva_gqa_kvcache(q, kn, vn, c["k_cache"], c["v_cache"], sk, out, H, Hkv, c["cos"],
+                            c["sin"], stream=s)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step(c["q"], c["k_new"], c["v_new"], c["seqlens_k"], stream)
+    torch.cuda.synchronize(dev)
+    if pva.pva_get_status(stream) != 0:
+        raise SystemExit("device status bits set during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    kernel_ms = []
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    pva.pva_profile(True)
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            starts[i].record(stream)
+            step(c["q"], c["k_new"], c["v_new"], c["seqlens_k"], stream)
+            ends[i].record(stream)
+            kernel_ms.append(pva.pva_kernel_times())
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    pva.pva_profile(False)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps,
+                        world, dev)
+    job_kv = sum_over_ranks(kv_bytes, world, dev)
+    if pva.pva_get_status(stream) != 0:
+        raise SystemExit("device status bits set during the timed steps")
+
+    # end to end: this step's new token (q, k, v) and lengths from pinned host
+    # memory, the output back; the caches stay resident, as in serving
+    host = {k: c[k].cpu().pin_memory() for k in ("q", "k_new", "v_new", "seqlens_k")}
+    dbuf = {k: torch.empty_like(c[k]) for k in host}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            flush.fill_(i & 0xff)
+            a.record(stream)
+            for k_ in host:
+                dbuf[k_].copy_(host[k_], non_blocking=True)
+            step(dbuf["q"], dbuf["k_new"], dbuf["v_new"], dbuf["seqlens_k"], stream)
+            out_host.copy_(out, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            if i >= args.warmup:
+                e2e_ms.append(a.elapsed_time(b))
+    e2e = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world, dev)
+    if pva.pva_get_status(stream) != 0:
+        raise SystemExit("device status bits set during the end-to-end steps")
+
+    peaks = measured_peaks()
+    dec_ms = [k[2] for k in kernel_ms if k[2] >= 0]
+    front_ms = [k[0] for k in kernel_ms]
+    dom_ms = sum(dec_ms) / len(dec_ms)
+    achieved = kv_bytes / (dom_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": job_kv / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[w_name], "name": w_name,
+                   **({"batch_override": args.batch} if args.batch else {}),
+                   "l2": "flushed between steps; caches (8.6 GB) exceed L2",
+                   "kv_bytes_per_step": kv_bytes,
+                   "kernel_ms": {"front_and_scheduler": sum(front_ms) / len(front_ms),
+                                 "decode": dom_ms},
+                   "parallelism": f"replicas x{world} (independent caches per GPU)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": recorded_traffic("decode_kvcache_bf16_d128_g4"),
+                     "kernel": "pva_decode_kernel (cache planes)",
+                     "peak_source": peaks["source"] + " hbm_gbs"},
+        "e2e": {"value": job_kv / (e2e * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
+        # metadata, append + rotary, scheduler, prefill (no items), decode
+        "gpu_launches": 5 * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w_name)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
 
 
 def main():
@@ -333,6 +515,9 @@ def main():
     pva.load_library()
 
     w_name = args.workload
+    if w_name == "bf16_kvcache_decode":
+        bench_kvcache(args, rank, world, local, dev)
+        return
     w = workloads.make(w_name, seed=rank, device=str(dev), B=args.batch)
     H, Hkv, d, dv = w["num_heads"], w["kv_num_heads"], w["head_size"], w["v_head_size"]
     flops, kv_bytes = work_units(w)

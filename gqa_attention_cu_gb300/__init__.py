@@ -15,7 +15,7 @@ import threading
 
 from . import workloads  # noqa: F401  (seeded synthetic inputs)
 
-__all__ = ["pva_forward", "pva_forward_local", "pva_forward_padded", "pva_get_status", "pva_schedule", "pva_status_string",
+__all__ = ["pva_forward", "pva_forward_local", "pva_forward_padded", "pva_gqa_kvcache", "pva_get_status", "pva_schedule", "pva_status_string",
            "pva_last_error", "pva_release", "pva_version", "pva_profile", "pva_kernel_times",
            "pva_selftest_wait", "load_library", "build", "PvaError", "DTYPE_CODES", "DEV_FLAGS"]
 
@@ -25,7 +25,8 @@ LIB_PATH = os.path.join(_PKG, "libpva.so")
 PVA_OK, PVA_ERR_INVALID_ARG, PVA_ERR_UNSUPPORTED, PVA_ERR_CUDA, PVA_ERR_OOM = 0, -1, -2, -3, -4
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
 DEV_FLAGS = {"cu_q_start": 0x1, "cu_kv_start": 0x2, "cu_q_order": 0x4, "cu_kv_order": 0x8,
-             "too_many": 0x10, "null_tensor": 0x20, "kv_len": 0x40, "wait_timeout": 0x100}
+             "too_many": 0x10, "null_tensor": 0x20, "kv_len": 0x40, "kv_cache": 0x80,
+             "wait_timeout": 0x100}
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +64,9 @@ def load_library(path: str | None = None):
         lib.pva_forward_padded.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, f, i,
                                            vp]
         lib.pva_forward_padded.restype = i
+        lib.pva_gqa_kvcache.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i,
+                                        i, i, i, i, i, f, f, i, i, vp]
+        lib.pva_gqa_kvcache.restype = i
         lib.pva_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.pva_get_status.restype = i
         lib.pva_schedule.argtypes = [vp, vp, i, i, i, i, i, i, i,
@@ -159,6 +163,39 @@ def pva_forward_padded(q, k, v, nonpad_kv_seqlen, out, B: int, q_seq: int, kv_se
                                 int(kv_seq), int(num_heads), int(kv_num_heads), int(head_size),
                                 int(v_head_size), float(scale), int(is_causal), float(softcap),
                                 code, _stream_ptr(stream))
+    _check(rc)
+
+
+def _ptr_or_none(t):
+    return None if t is None else t.data_ptr()
+
+
+def pva_gqa_kvcache(q, k_new, v_new, k_cache, v_cache, seqlens_k, out, num_heads: int,
+                    kv_num_heads: int, cos_cache=None, sin_cache=None, position_ids=None,
+                    rotary_interleaved: bool = False, scale: float = 0.0, softcap: float = 0.0,
+                    local_window: int = 0, dtype: int | None = None, stream=None) -> None:
+    """One GroupQueryAttention step on a fixed-capacity BNSH cache: q
+    [B, q_seq, H, d], k_new/v_new [B, k_seq, Hkv, d] (or None), caches
+    [B, Hkv, capacity, d] (appended in place), seqlens_k int32 [B] (= keys
+    after the step - 1), optional cos/sin tables [rows, rotary_dim/2] and
+    position_ids int64 [B, q_seq]; out [B, q_seq, H, d]."""
+    lib = load_library()
+    code = _dtype_code(q) if dtype is None else int(dtype)
+    B, q_seq, _, d = q.shape
+    k_seq = 0 if k_new is None else int(k_new.shape[1])
+    capacity = int(k_cache.shape[2])
+    rot = rows = 0
+    rot_code = 0
+    if cos_cache is not None:
+        rows, rot = int(cos_cache.shape[0]), 2 * int(cos_cache.shape[1])
+        rot_code = _dtype_code(cos_cache)
+    rc = lib.pva_gqa_kvcache(q.data_ptr(), _ptr_or_none(k_new), _ptr_or_none(v_new),
+                             k_cache.data_ptr(), v_cache.data_ptr(), seqlens_k.data_ptr(),
+                             _ptr_or_none(cos_cache), _ptr_or_none(sin_cache),
+                             _ptr_or_none(position_ids), out.data_ptr(), int(B), int(q_seq),
+                             k_seq, capacity, int(num_heads), int(kv_num_heads), int(d), rot,
+                             rows, int(bool(rotary_interleaved)), rot_code, float(scale),
+                             float(softcap), int(local_window), code, _stream_ptr(stream))
     _check(rc)
 
 

@@ -17,7 +17,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpva.so")
 
 SOURCES = ["pva_api.cu", "pva_scheduler.cu", "pva_prefill_f32.cu", "pva_prefill_tc.cu",
-           "pva_prefill_pair.cu", "pva_decode.cu", "pva_noalloc.cu"]
+           "pva_prefill_pair.cu", "pva_decode.cu", "pva_noalloc.cu", "pva_kvcache.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

@@ -117,6 +117,30 @@ int encode_map(CUtensorMap* map, const void* base, int dtype, int dim, int heads
   return PVA_OK;
 }
 
+// Rank-3 map over a BNSH cache [planes, rows, dim] (plane = sequence * Hkv +
+// kv head, rows = the cache capacity): boxes of box_rows rows of one plane.
+// Rows past the capacity read as zeros.
+int encode_plane_map(CUtensorMap* map, const void* base, int dtype, int dim, int rows,
+                     long long planes, int box_dim, int box_rows, bool swizzle128) {
+  const cuuint64_t gdim[3] = {(cuuint64_t)dim, (cuuint64_t)rows, (cuuint64_t)planes};
+  const cuuint64_t gstride[2] = {(cuuint64_t)dim * 2, (cuuint64_t)dim * rows * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)box_dim, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = g_encode(map, dtype == PVA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void*>(base), gdim, gstride, box, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char msg[160];
+    snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled failed (%d) dim=%d rows=%d planes=%lld",
+             (int)r, dim, rows, planes);
+    return fail(PVA_ERR_CUDA, msg);
+  }
+  return PVA_OK;
+}
+
 int check_and_plan(const void* q, const void* k, const void* v, const int32_t* cu_q,
                    const int32_t* cu_kv, void* out, int B, int H, int Hkv, int d, int dv,
                    float scale, float softcap, int dtype, Plan* plan) {
@@ -256,31 +280,70 @@ int prepare(const void* q, const void* k, const void* v, const int32_t* cu_q,
   return PVA_OK;
 }
 
-// Body shared by the entry points.  `nonpad` (padded layout, device int64 [B])
-// selects the padded form: the offsets and key lengths are then built on the
-// device from q_seq, kv_seq and nonpad, and cu_seqlens_q/kv are ignored.
-int forward_impl(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
-                 const int32_t* cu_seqlens_kv, void* out, int B, int num_heads,
-                 int kv_num_heads, int head_size, int v_head_size, float scale, int is_causal,
-                 float softcap, int local_window, int dtype, void* stream_,
-                 const int64_t* nonpad, int q_seq, int kv_seq) {
+// What one call computes, whichever entry point it came through.
+struct Spec {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* cu_q;
+  const int32_t* cu_kv;
+  void* out;
+  int B, H, Hkv, d, dv;
+  float scale;
+  int is_causal;
+  float softcap;
+  int window;
+  int dtype;
+  // padded form (pva_forward_padded): device int64 [B]; offsets built on the device
+  const int64_t* nonpad = nullptr;
+  int q_seq = 0, kv_seq = 0;
+  // cache form (pva_gqa_kvcache): front end and K/V read from the cache planes
+  const CacheStep* cache = nullptr;
+};
+
+int forward_impl(const Spec& s, void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   std::lock_guard<std::mutex> lock(g_mu);
   Plan plan;
   AttnParams p{};
   int num_sms = 0;
-  const size_t front_words = nonpad ? 3 * (size_t)(B > 0 ? B : 0) + 2 : 0;
-  int rc = prepare(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B, num_heads, kv_num_heads,
-                   head_size, v_head_size, scale, is_causal, softcap, dtype, stream, &plan, &p,
-                   &num_sms, front_words);
+  const int B = s.B;
+  const size_t elt = s.dtype == PVA_F32 ? 4 : 2;
+  // Library-built offsets sit after the work lists: [cu_q B+1][cu_kv B+1]
+  // [kv_len B] (+ [past B][first query B] for the cache form), then, for a
+  // rotary cache step, the rotated queries.
+  size_t front_words = 0, qrot_bytes = 0;
+  if (s.nonpad) front_words = 3 * (size_t)B + 2;
+  if (s.cache) {
+    front_words = ((5 * (size_t)B + 2 + 63) / 64) * 64;
+    if (s.cache->rot > 0) qrot_bytes = (size_t)B * s.cache->q_seq * s.H * s.d * elt;
+  }
+  int rc = prepare(s.q, s.k, s.v, s.cu_q, s.cu_kv, s.out, B, s.H, s.Hkv, s.d, s.dv, s.scale,
+                   s.is_causal, s.softcap, s.dtype, stream, &plan, &p, &num_sms,
+                   front_words + (qrot_bytes + 3) / 4);
   if (rc != PVA_OK) return rc;
-  p.window = local_window > 0 ? local_window : 0;
-  int32_t* front = nullptr;
-  if (nonpad) {
-    front = p.ws + WsLayout{B, kv_num_heads}.int_words();
+  p.window = s.window > 0 ? s.window : 0;
+  int32_t* front = p.ws + WsLayout{B, s.Hkv}.int_words();
+  CacheStep cs{};
+  if (s.nonpad) {
     p.cu_q = front;
     p.cu_kv = front + B + 1;
     p.kv_len = front + 2 * B + 2;
+  }
+  if (s.cache) {
+    cs = *s.cache;
+    cs.cu_q = front;
+    cs.cu_kv = front + B + 1;
+    cs.kv_len = front + 2 * B + 2;
+    cs.past = front + 3 * B + 2;
+    cs.q_first = front + 4 * B + 2;
+    cs.status = p.status;
+    cs.q_rot = qrot_bytes ? static_cast<void*>(front + front_words) : nullptr;
+    p.cu_q = cs.cu_q;
+    p.cu_kv = cs.cu_kv;
+    p.kv_len = cs.kv_len;
+    p.kv_cap = cs.cap;
+    if (cs.q_rot) p.q = cs.q_rot;
   }
 
   CUtensorMap tq, tk, tv, to, dk, dvm;
@@ -289,24 +352,40 @@ int forward_impl(const void* q, const void* k, const void* v, const int32_t* cu_
     // An empty tensor may come as NULL; its map is never used (the device
     // check empties the work lists), but the encoder wants a real address.
     const void* any = p.ws;
-    if (!q) q = any;
-    if (!k) k = any;
-    if (!v) v = any;
-    void* o = out ? out : p.ws;
-    const int G = p.G, m = kTcRows / G, bn = tc_block_n(head_size, v_head_size);
-    if ((rc = encode_map(&tq, q, dtype, head_size, num_heads, 64, G, m, true)) != PVA_OK ||
-        (rc = encode_map(&tk, k, dtype, head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK ||
-        (rc = encode_map(&tv, v, dtype, v_head_size, kv_num_heads, 64, 1, bn, true)) != PVA_OK ||
-        (rc = encode_map(&to, o, dtype, v_head_size, num_heads, 64, G, out_box_tokens(G),
-                         true)) != PVA_OK)
+    const void* q = p.q ? p.q : any;
+    const void* k = s.k ? s.k : any;
+    const void* v = s.v ? s.v : any;
+    void* o = s.out ? s.out : p.ws;
+    const int G = p.G, m = kTcRows / G, bn = tc_block_n(s.d, s.dv);
+    if ((rc = encode_map(&tq, q, s.dtype, s.d, s.H, 64, G, m, true)) != PVA_OK ||
+        (rc = encode_map(&to, o, s.dtype, s.dv, s.H, 64, G, out_box_tokens(G), true)) !=
+            PVA_OK)
       return rc;
-    if (plan.decode) {
-      const int tkeys = decode_tile_keys(head_size);
-      if ((rc = encode_map(&dk, k, dtype, head_size, kv_num_heads, head_size, 1, tkeys,
-                           false)) != PVA_OK ||
-          (rc = encode_map(&dvm, v, dtype, v_head_size, kv_num_heads, v_head_size, 1, tkeys,
-                           false)) != PVA_OK)
+    if (s.cache) {
+      const long long planes = (long long)B * s.Hkv;
+      if ((rc = encode_plane_map(&tk, k, s.dtype, s.d, cs.cap, planes, 64, bn, true)) !=
+              PVA_OK ||
+          (rc = encode_plane_map(&tv, v, s.dtype, s.dv, cs.cap, planes, 64, bn, true)) !=
+              PVA_OK)
         return rc;
+      if (plan.decode) {
+        const int tkeys = decode_tile_keys(s.d);
+        if ((rc = encode_plane_map(&dk, k, s.dtype, s.d, cs.cap, planes, s.d, tkeys,
+                                   false)) != PVA_OK ||
+            (rc = encode_plane_map(&dvm, v, s.dtype, s.dv, cs.cap, planes, s.dv, tkeys,
+                                   false)) != PVA_OK)
+          return rc;
+      }
+    } else {
+      if ((rc = encode_map(&tk, k, s.dtype, s.d, s.Hkv, 64, 1, bn, true)) != PVA_OK ||
+          (rc = encode_map(&tv, v, s.dtype, s.dv, s.Hkv, 64, 1, bn, true)) != PVA_OK)
+        return rc;
+      if (plan.decode) {
+        const int tkeys = decode_tile_keys(s.d);
+        if ((rc = encode_map(&dk, k, s.dtype, s.d, s.Hkv, s.d, 1, tkeys, false)) != PVA_OK ||
+            (rc = encode_map(&dvm, v, s.dtype, s.dv, s.Hkv, s.dv, 1, tkeys, false)) != PVA_OK)
+          return rc;
+      }
     }
   }
 
@@ -318,10 +397,14 @@ int forward_impl(const void* q, const void* k, const void* v, const int32_t* cu_
   }
   prof_mark(0, stream);
   cudaError_t e = cudaSuccess;
-  if (nonpad) {
-    e = launch_padded_front(nonpad, B, q_seq, kv_seq, front, front + B + 1, front + 2 * B + 2,
-                            stream);
+  if (s.nonpad) {
+    e = launch_padded_front(s.nonpad, B, s.q_seq, s.kv_seq, front, front + B + 1,
+                            front + 2 * B + 2, stream);
     if (e != cudaSuccess) return cuda_fail(e, "padded front-end launch");
+  }
+  if (s.cache) {
+    e = launch_cache_front(cs, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kv-cache front-end launch");
   }
   e = launch_scheduler(p, plan.sched, stream);
   if (e != cudaSuccess) return cuda_fail(e, "scheduler launch");
@@ -332,13 +415,12 @@ int forward_impl(const void* q, const void* k, const void* v, const int32_t* cu_
     prof_mark(2, stream);
     return PVA_OK;
   }
-  e = tc_paired(head_size, v_head_size)
-          ? launch_prefill_pair(p, dtype, tq, tk, tv, to, num_sms, stream)
-          : launch_prefill_tc(p, dtype, tq, tk, tv, num_sms, stream);
+  e = tc_paired(s.d, s.dv) ? launch_prefill_pair(p, s.dtype, tq, tk, tv, to, num_sms, stream)
+                           : launch_prefill_tc(p, s.dtype, tq, tk, tv, num_sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
   prof_mark(2, stream);
   if (plan.decode) {
-    e = launch_decode(p, dtype, dk, dvm, num_sms, stream);
+    e = launch_decode(p, s.dtype, dk, dvm, num_sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "split-KV decode launch");
     prof_mark(3, stream);
   }
@@ -353,18 +435,18 @@ int pva_forward(const void* q, const void* k, const void* v, const int32_t* cu_s
                 const int32_t* cu_seqlens_kv, void* out, int B, int num_heads, int kv_num_heads,
                 int head_size, int v_head_size, float scale, int is_causal, float softcap,
                 int dtype, void* stream) {
-  return forward_impl(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B, num_heads, kv_num_heads,
-                      head_size, v_head_size, scale, is_causal, softcap, 0, dtype, stream,
-                      nullptr, 0, 0);
+  const Spec s{q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B, num_heads, kv_num_heads,
+               head_size, v_head_size, scale, is_causal, softcap, 0, dtype};
+  return forward_impl(s, stream);
 }
 
 int pva_forward_local(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
                       const int32_t* cu_seqlens_kv, void* out, int B, int num_heads,
                       int kv_num_heads, int head_size, int v_head_size, float scale,
                       int is_causal, float softcap, int local_window, int dtype, void* stream) {
-  return forward_impl(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B, num_heads, kv_num_heads,
-                      head_size, v_head_size, scale, is_causal, softcap, local_window, dtype,
-                      stream, nullptr, 0, 0);
+  const Spec s{q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B, num_heads, kv_num_heads,
+               head_size, v_head_size, scale, is_causal, softcap, local_window, dtype};
+  return forward_impl(s, stream);
 }
 
 int pva_forward_padded(const void* q, const void* k, const void* v,
@@ -380,9 +462,72 @@ int pva_forward_padded(const void* q, const void* k, const void* v,
   // The offsets are built on the device; the nonpad pointer stands in for them
   // in the host checks (which only test that they are non-null).
   const int32_t* stand_in = reinterpret_cast<const int32_t*>(nonpad_kv_seqlen);
-  return forward_impl(q, k, v, stand_in, stand_in, out, B, num_heads, kv_num_heads, head_size,
-                      v_head_size, scale, is_causal, softcap, 0, dtype, stream,
-                      nonpad_kv_seqlen, q_seq, kv_seq);
+  Spec s{q, k, v, stand_in, stand_in, out, B, num_heads, kv_num_heads, head_size,
+         v_head_size, scale, is_causal, softcap, 0, dtype};
+  s.nonpad = nonpad_kv_seqlen;
+  s.q_seq = q_seq;
+  s.kv_seq = kv_seq;
+  return forward_impl(s, stream);
+}
+
+int pva_gqa_kvcache(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                    void* v_cache, const int32_t* seqlens_k, const void* cos_cache,
+                    const void* sin_cache, const int64_t* position_ids, void* out, int B,
+                    int q_seq, int k_seq, int capacity, int num_heads, int kv_num_heads,
+                    int head_size, int rotary_dim, int cache_rows, int rotary_interleaved,
+                    int rotary_dtype, float scale, float softcap, int local_window, int dtype,
+                    void* stream) {
+  if (!q || !k_cache || !v_cache || !out || !seqlens_k)
+    return fail(PVA_ERR_INVALID_ARG, "null q, cache, out or seqlens_k pointer");
+  if (B < 1 || q_seq < 1 || k_seq < 0 || capacity < 1)
+    return fail(PVA_ERR_INVALID_ARG, "need B >= 1, q_seq >= 1, k_seq >= 0, capacity >= 1");
+  if (k_seq > 0 && (!k_new || !v_new))
+    return fail(PVA_ERR_INVALID_ARG, "null k_new or v_new with k_seq > 0");
+  if ((long long)(B + 1) * capacity > INT_MAX - 65536 || (long long)B * q_seq > INT_MAX ||
+      (long long)B * k_seq > INT_MAX)
+    return fail(PVA_ERR_INVALID_ARG, "cache or token extents do not fit in int32");
+  if (head_size % 2 != 0) return fail(PVA_ERR_UNSUPPORTED, "head_size must be even");
+  if (rotary_dim != 0) {
+    if (rotary_dim < 2 || rotary_dim % 2 != 0 || rotary_dim > head_size)
+      return fail(PVA_ERR_INVALID_ARG, "rotary_dim must be even with 2 <= rotary_dim <= head_size");
+    if (!cos_cache || !sin_cache || cache_rows < 1)
+      return fail(PVA_ERR_INVALID_ARG, "rotary embedding needs cos/sin tables with rows >= 1");
+    if ((long long)cache_rows * (rotary_dim / 2) > INT_MAX)
+      return fail(PVA_ERR_INVALID_ARG, "cos/sin tables too large");
+    if (k_seq != 0 && k_seq != q_seq)
+      return fail(PVA_ERR_INVALID_ARG, "rotary embedding needs k_seq == q_seq (or k_seq == 0)");
+    if (rotary_dtype != PVA_F32 && !(rotary_dtype == PVA_F16 && dtype != PVA_F32))
+      return fail(PVA_ERR_INVALID_ARG,
+                  "cos/sin tables must be f32, or f16 with f16/bf16 queries");
+  }
+  CacheStep c{};
+  c.q = q;
+  c.k_new = k_new;
+  c.v_new = v_new;
+  c.k_cache = k_cache;
+  c.v_cache = v_cache;
+  c.seqlens_k = seqlens_k;
+  c.cos_cache = cos_cache;
+  c.sin_cache = sin_cache;
+  c.position_ids = position_ids;
+  c.B = B;
+  c.q_seq = q_seq;
+  c.k_seq = k_seq;
+  c.cap = capacity;
+  c.H = num_heads;
+  c.Hkv = kv_num_heads;
+  c.d = head_size;
+  c.rot = rotary_dim;
+  c.cache_rows = cache_rows;
+  c.interleaved = rotary_interleaved ? 1 : 0;
+  c.rot_f16 = rotary_dtype == PVA_F16 ? 1 : 0;
+  c.dtype = dtype;
+  // The attention reads the cache planes; seqlens_k stands in for the offsets
+  // in the host checks (which only test that they are non-null).
+  Spec s{q, k_cache, v_cache, seqlens_k, seqlens_k, out, B, num_heads, kv_num_heads,
+         head_size, head_size, scale, 1, softcap, local_window, dtype};
+  s.cache = &c;
+  return forward_impl(s, stream);
 }
 
 int pva_get_status(void* stream_, uint32_t* device_flags) {

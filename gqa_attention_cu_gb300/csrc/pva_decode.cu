@@ -27,6 +27,7 @@
 //               combine) and writes the output, so results do not depend on
 //               which CTA finishes last.
 #include "pva_device.cuh"
+#include "pva_items.cuh"
 
 namespace pva {
 namespace {
@@ -89,6 +90,20 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, const SchedHead
   r.ks = min(lkv, kbeg + r.s * per);
   r.ke = min(lkv, r.ks + per);
   return r;
+}
+
+// First row (packed row index) of tile j of a unit.  Packed K/V: tiles are
+// shifted back only at the end of the tensor (rows past the unit are other
+// sequences' keys, weighted 0).  Cache planes: the unit's last tile is shifted
+// back to end at the unit's last key -- before row 0 of the plane, where the
+// tensor copy reads zeros, if the unit is shorter than a tile -- so no row
+// past the sequence's keys, which holds whatever the cache held, is ever
+// loaded.  The rows a shifted tile repeats are masked as already seen.
+template <int TK>
+__device__ __forceinline__ int tile_row(const AttnParams& p, const Unit& un, int j,
+                                        int total_kv) {
+  const int lim = p.kv_cap ? un.kv_start + un.ke : total_kv;
+  return min(un.kv_start + un.ks + j * TK, lim - TK);
 }
 
 __device__ __forceinline__ void compute_bar_sync() {
@@ -157,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t* status = p.status;
   volatile int* abort = &s_abort;
-  const int total_kv = p.cu_kv[p.B];
+  const int total_kv = kv_tile_end(p);
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -203,11 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < nt; ++j, ++cnt) {
           const int st = cnt % kStages;
           if (!(ok = mbar_wait(&empty[st], ((cnt / kStages) & 1) ^ 1, abort, status))) break;
-          const int k0 = min(un.kv_start + un.ks + j * TK, total_kv - TK);
+          const int k0 = tile_row<TK>(p, un, j, total_kv);
           uint8_t* dk = smem + C::OFF_KV + st * 2 * C::TILE_BYTES;
           mbar_arrive_expect_tx(&full[st], 2 * C::TILE_BYTES);
-          tma_load_3d(dk, &tmap_k, &full[st], 0, un.g, k0);
-          tma_load_3d(dk + C::TILE_BYTES, &tmap_v, &full[st], 0, un.g, k0);
+          const int2 yz = kv_tma_yz(p, un.b, un.g, un.kv_start, k0);
+          tma_load_3d(dk, &tmap_k, &full[st], 0, yz.x, yz.y);
+          tma_load_3d(dk + C::TILE_BYTES, &tmap_v, &full[st], 0, yz.x, yz.y);
         }
       }
       if (ok) {
@@ -271,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const uint8_t* sK = smem + C::OFF_KV + st * 2 * C::TILE_BYTES;
         const uint8_t* sV = sK + C::TILE_BYTES;
-        const int k0 = min(un.kv_start + un.ks + j * TK, total_kv - TK);
+        const int k0 = tile_row<TK>(p, un, j, total_kv);
         const int base = k0 - un.kv_start;            // local key of tile row 0
         const int lo = un.ks + j * TK - base;          // visible tile rows [lo, hi)
         const int hi = min(un.ks + (j + 1) * TK, un.ke) - base;

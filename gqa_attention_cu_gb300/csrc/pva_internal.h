@@ -88,6 +88,10 @@ struct AttnParams {
   // start of its slot [cu_kv[b], cu_kv[b+1]) (padded K/V); nullptr: the whole
   // slot is the sequence.
   const int32_t* kv_len;
+  // > 0: K and V are a BNSH cache [B, Hkv, kv_cap, d] (one plane of kv_cap
+  // rows per (sequence, kv head)) and cu_kv[b] = b * kv_cap; 0: packed
+  // [tokens, Hkv, d].
+  int kv_cap;
   int B, H, Hkv, G, d, dv;
   float scale;    // resolved (default already applied)
   float softcap;  // 0 = off
@@ -148,6 +152,31 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size
 
 // ---- launchers (defined next to their kernels) -------------------------------
 cudaError_t launch_scheduler(const AttnParams& p, const SchedConfig& c, cudaStream_t s);
+// One GroupQueryAttention step against a fixed-capacity BNSH KV cache (the
+// front end of pva_gqa_kvcache): metadata, in-place append and rotary
+// embedding, before the attention kernels read the cache.
+struct CacheStep {
+  const void* q;        // [B, q_seq, H, d]
+  const void* k_new;    // [B, k_seq, Hkv, d]
+  const void* v_new;    // [B, k_seq, Hkv, d]
+  void* k_cache;        // [B, Hkv, cap, d], appended in place
+  void* v_cache;
+  const int32_t* seqlens_k;  // [B]: valid keys after the append, minus one
+  const void* cos_cache;     // [cache_rows, rot / 2], f32 or f16
+  const void* sin_cache;
+  const int64_t* position_ids;  // [B, q_seq] or nullptr
+  void* q_rot;          // [B, q_seq, H, d] rotated queries (rot > 0)
+  int32_t* cu_q;        // [B + 1] out: b * q_seq
+  int32_t* cu_kv;       // [B + 1] out: b * cap
+  int32_t* kv_len;      // [B] out: total keys, or -1 (step rejected)
+  int32_t* past;        // [B] out: first appended row, or -1
+  int32_t* q_first;     // [B] out: position of the first query row, or -1
+  uint32_t* status;
+  int B, q_seq, k_seq, cap, H, Hkv, d;
+  int rot, cache_rows, interleaved, rot_f16, dtype;
+};
+cudaError_t launch_cache_front(const CacheStep& c, cudaStream_t s);
+
 cudaError_t launch_padded_front(const int64_t* nonpad, int B, int q_seq, int kv_seq,
                                 int32_t* cu_q, int32_t* cu_kv, int32_t* kv_len, cudaStream_t s);
 cudaError_t launch_prefill_f32(const AttnParams& p, int num_sms, cudaStream_t s);

@@ -47,6 +47,38 @@ __device__ __forceinline__ PrefillItem decode_prefill_item(const AttnParams& p,
   return r;
 }
 
+// K/V addressing.  Packed K/V [tokens, Hkv, d]: key row k0 (a token index)
+// of kv head g sits at TMA coordinates (y, z) = (g, k0).  BNSH cache: plane
+// b * Hkv + g, row k0 - kv_start, so (y, z) = (k0 - kv_start, b * Hkv + g).
+__device__ __forceinline__ int2 kv_tma_yz(const AttnParams& p, int b, int g, int kv_start,
+                                          int k0) {
+  return p.kv_cap ? make_int2(k0 - kv_start, b * p.Hkv + g) : make_int2(g, k0);
+}
+
+// Largest token index + 1 a key tile may reach.  Packed tiles are clamped
+// inside the tensor; a cache plane is zero-filled past its capacity by the
+// tensor copy, so cache tiles are never shifted (the host keeps
+// (B + 1) * kv_cap far below INT_MAX).
+__device__ __forceinline__ int kv_tile_end(const AttnParams& p) {
+  return p.kv_cap ? INT_MAX : p.cu_kv[p.B];
+}
+
+// End (exclusive packed row) a sequence's key tiles are shifted back to.
+// Packed K/V: the end of the tensor.  Cache planes: the sequence's last key,
+// so that its last tile ends there (starting before row 0, where the tensor
+// copy reads zeros, for a sequence shorter than a tile) and no row past its
+// keys -- whatever the cache holds there -- is ever loaded.  Columns a shifted
+// tile repeats are masked as already seen.
+__device__ __forceinline__ int key_tile_limit(const AttnParams& p, int kv_start, int lkv,
+                                              int total_kv) {
+  return p.kv_cap ? kv_start + lkv : total_kv;
+}
+
+// Row index (in units of head rows) of local key j of kv head g, sequence b.
+__device__ __forceinline__ size_t kv_row(const AttnParams& p, int b, int kv_start, int g, int j) {
+  return p.kv_cap ? (size_t)(b * p.Hkv + g) * p.kv_cap + j : (size_t)(kv_start + j) * p.Hkv + g;
+}
+
 // First local key an item must visit: 0, or with a local window W the window
 // start of its first query row (later rows start later).
 __device__ __forceinline__ int item_key_begin(const PrefillItem& it, int tile_tokens, int window) {

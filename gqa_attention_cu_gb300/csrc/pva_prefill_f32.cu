@@ -70,11 +70,11 @@ __global__ void __launch_bounds__(kWarps * 32) pva_prefill_f32_kernel(AttnParams
       for (int e = threadIdx.x; e < kF32KeyTile * d; e += blockDim.x) {
         const int j = e / d, c = e - j * d;
         sk[j * kstride + c] =
-            j < nk ? K[((size_t)(item.kv_start + k0 + j) * p.Hkv + g) * d + c] : 0.0f;
+            j < nk ? K[kv_row(p, item.b, item.kv_start, g, k0 + j) * d + c] : 0.0f;
       }
       for (int e = threadIdx.x; e < kF32KeyTile * dv; e += blockDim.x) {
         const int j = e / dv, c = e - j * dv;
-        sv[e] = j < nk ? V[((size_t)(item.kv_start + k0 + j) * p.Hkv + g) * dv + c] : 0.0f;
+        sv[e] = j < nk ? V[kv_row(p, item.b, item.kv_start, g, k0 + j) * dv + c] : 0.0f;
       }
       __syncthreads();
 

@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.G;
   const int m_tok = kTcRows / G;  // tokens per query tile (the item covers 2 m)
   const int total_q = p.cu_q[p.B];
-  const int total_kv = p.cu_kv[p.B];
+  const int total_kv = kv_tile_end(p);
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -285,7 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         c * 64, g * G, v.q0 + t * m_tok);
         ++items;
         for (int j = 0; ok && j < v.n_tiles; ++j) {
-          const int k0 = min(v.kv_start + (v.jb + j) * BN, total_kv - BN);
+          const int k0 = min(v.kv_start + (v.jb + j) * BN,
+                             key_tile_limit(p, v.kv_start, v.lkv, total_kv) - BN);
+          const int2 yz = kv_tma_yz(p, it.b, g, v.kv_start, k0);
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv, ++loads) {
             const int sl = loads % C::SLOTS;
@@ -297,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < C::KCH; ++c)
               tma_load_3d(dst + c * C::KV_CHUNK, kv ? &tmap_v : &tmap_k, &bars->ring_full[sl],
-                          c * 64, g, k0);
+                          c * 64, yz.x, yz.y);
           }
         }
       }
@@ -468,7 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const int J = it.jb + j;            // key tile index within the sequence
-        const int k0 = min(it.kv_start + J * BN, total_kv - BN);
+        const int k0 = min(it.kv_start + J * BN,
+                           key_tile_limit(p, it.kv_start, it.lkv, total_kv) - BN);
         const int base = k0 - it.kv_start;  // local key index of column 0
         const int lo_c = max(J * BN, row_lo) - base;  // visible columns [lo_c, hi_c)
         const int hi_c = min((J + 1) * BN, row_hi) - base;

@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.G;
   const int m_tok = kTcRows / G;  // tokens per query tile (one tile per item)
   const int total_q = p.cu_q[p.B];
-  const int total_kv = p.cu_kv[p.B];
+  const int total_kv = kv_tile_end(p);
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -263,7 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sQ + c * C::Q_CHUNK, &tmap_q, &bars->q_full, c * 64, g * G, v.q0);
         ++q_cnt;
         for (int j = 0; ok && j < v.n_tiles; ++j) {
-          const int k0 = min(v.kv_start + (v.jb + j) * BN, total_kv - BN);
+          const int k0 = min(v.kv_start + (v.jb + j) * BN,
+                             key_tile_limit(p, v.kv_start, v.lkv, total_kv) - BN);
+          const int2 yz = kv_tma_yz(p, it.b, g, v.kv_start, k0);
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv, ++loads) {
             const int sl = loads % C::SLOTS;
@@ -275,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nch = kv ? C::VCH : C::KCH;
             for (int c = 0; c < nch; ++c)
               tma_load_3d(dst + c * C::KV_CHUNK, kv ? &tmap_v : &tmap_k, &bars->ring_full[sl],
-                          c * 64, g, k0);
+                          c * 64, yz.x, yz.y);
           }
         }
       }
@@ -434,7 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(t_lane + col_s + 32, vb);
         tmem_wait_ld();
         const int J = it.jb + j;            // key tile index within the sequence
-        const int k0 = min(it.kv_start + J * BN, total_kv - BN);
+        const int k0 = min(it.kv_start + J * BN,
+                           key_tile_limit(p, it.kv_start, it.lkv, total_kv) - BN);
         const int base = k0 - it.kv_start;  // local key index of column 0
         const int lo_c = max(J * BN, row_lo) - base;  // visible columns [lo_c, hi_c)
         const int hi_c = min((J + 1) * BN, row_hi) - base;

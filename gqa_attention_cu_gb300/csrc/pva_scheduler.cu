@@ -234,7 +234,9 @@ __global__ void __launch_bounds__(NT) pva_schedule_kernel(AttnParams p, SchedCon
     const int lkv = p.kv_len ? p.kv_len[b] : slot;
     if (lq < 0) atomicOr(&s_status, PVA_DEV_CU_Q_ORDER);
     if (slot < 0) atomicOr(&s_status, PVA_DEV_CU_KV_ORDER);
-    if (lkv < 0 || lkv > slot) atomicOr(&s_status, PVA_DEV_KV_LEN);
+    // (a cache step the front end rejected comes with -1 lengths and has
+    // latched its own bit already)
+    if (lkv < 0 || lkv > slot) atomicOr(&s_status, p.kv_cap ? PVA_DEV_KV_CACHE : PVA_DEV_KV_LEN);
     if (staged) {
       s_lq[b] = lq;
       s_lkv[b] = lkv;

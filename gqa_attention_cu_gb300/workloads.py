@@ -79,6 +79,12 @@ WORKLOADS = {
                          "uniform_self", params={"lo": 512, "hi": 4096}),
     "bf16_window": Workload("bf16_window", 4, 32, 8, 128, 128, "bf16", True, 0.0, 0.0, 1.0,
                             "loguniform_self", params={"lo": 8192, "hi": 32768}, window=4096),
+    # one decode step against a fixed-capacity BNSH KV cache (pva_gqa_kvcache):
+    # totals after the append ~ U[lo, hi], rotary embedding on all 128 dims
+    "bf16_kvcache_decode": Workload("bf16_kvcache_decode", 256, 32, 8, 128, 128, "bf16", True,
+                                    0.0, 0.0, 1.0, "decode",
+                                    params={"lo": 512, "hi": 8192, "capacity": 8192,
+                                            "rotary_dim": 128, "cache_rows": 8192}),
 }
 
 
@@ -160,4 +166,43 @@ def make(name: str, seed: int = 0, shrink: int = 1, B: int | None = None,
         "head_size": w.head_size, "v_head_size": w.v_head_size,
         "dtype": w.dtype, "is_causal": w.is_causal, "scale": w.scale,
         "softcap": w.softcap, "sigma": w.sigma, "window": w.window,
+    }
+
+
+def rotary_tables(rows: int, rotary_dim: int, base: float = 10000.0, dtype=torch.float32):
+    """cos/sin tables [rows, rotary_dim/2]: angle p * base^(-k / (rotary_dim/2))."""
+    half = rotary_dim // 2
+    theta = base ** (-torch.arange(half, dtype=torch.float64) / half)
+    ang = torch.arange(rows, dtype=torch.float64)[:, None] * theta[None, :]
+    return torch.cos(ang).to(dtype), torch.sin(ang).to(dtype)
+
+
+def make_cache_step(name: str, seed: int = 0, B: int | None = None, device: str = "cpu"):
+    """Inputs of one decode step against a KV cache for workload ``name``:
+    q [B, 1, H, d], k_new/v_new [B, 1, Hkv, d], caches [B, Hkv, capacity, d]
+    (every row drawn, so rows past each total are finite), seqlens_k int32
+    [B] = totals - 1, rotary tables.  Totals come from a CPU generator seeded
+    with ``seed``; values from a generator on ``device`` seeded with seed + 1."""
+    w = WORKLOADS[name]
+    p = w.params
+    B = w.B if B is None else B
+    gen = torch.Generator("cpu")
+    gen.manual_seed(seed)
+    totals = torch.randint(p["lo"], p["hi"] + 1, (B,), generator=gen).tolist()
+    vg = torch.Generator(device)
+    vg.manual_seed(seed + 1)
+    td = DTYPES[w.dtype]
+    H, Hkv, d, cap = w.num_heads, w.kv_num_heads, w.head_size, p["capacity"]
+
+    def draw(*shape):
+        return (torch.randn(shape, generator=vg, device=device) * w.sigma).to(td)
+
+    cos, sin = rotary_tables(p["cache_rows"], p["rotary_dim"])
+    return {
+        "name": name, "B": B, "num_heads": H, "kv_num_heads": Hkv, "head_size": d,
+        "capacity": cap, "totals": totals,
+        "q": draw(B, 1, H, d), "k_new": draw(B, 1, Hkv, d), "v_new": draw(B, 1, Hkv, d),
+        "k_cache": draw(B, Hkv, cap, d), "v_cache": draw(B, Hkv, cap, d),
+        "seqlens_k": torch.tensor([t - 1 for t in totals], dtype=torch.int32, device=device),
+        "cos": cos.to(device), "sin": sin.to(device), "dtype": w.dtype,
     }

@@ -57,6 +57,8 @@ typedef enum { PVA_F32 = 0, PVA_F16 = 1, PVA_BF16 = 2 } pva_dtype;
 #define PVA_DEV_TOO_MANY 0x10u    /* work count does not fit the 32-bit work index */
 #define PVA_DEV_NULL_TENSOR 0x20u /* a NULL q/k/v/out with a nonzero token extent */
 #define PVA_DEV_KV_LEN 0x40u      /* pva_forward_padded: a nonpad length outside [0, kv_seq] */
+#define PVA_DEV_KV_CACHE 0x80u    /* pva_gqa_kvcache: a step outside the cache's bounds, or one
+                                     after such a step (see there) */
 #define PVA_DEV_WAIT_TIMEOUT 0x100u /* a pipeline wait in a kernel gave up (never expected) */
 
 /*
@@ -154,6 +156,63 @@ int pva_forward_padded(const void* q, const void* k, const void* v,
                        int kv_seq, int num_heads, int kv_num_heads, int head_size,
                        int v_head_size, float scale, int is_causal, float softcap,
                        int dtype, void* stream);
+
+/*
+ * pva_gqa_kvcache -- one GroupQueryAttention step against a fixed-capacity
+ * KV cache, as on the group_query_attention.rs page: the per-sequence
+ * metadata of `gqa_prepare_metadata`, the in-place append of
+ * `gqa_append_cache`, the rotary embedding of `gqa_rope_bnsh` (on the queries
+ * and on the appended keys), then causal attention of every query row over
+ * the sequence's valid cache rows, read straight from the BNSH cache.
+ *
+ * q       : [B, q_seq, num_heads, head_size]              (read)
+ * k_new, v_new : [B, k_seq, kv_num_heads, head_size]      (read; NULL if k_seq 0)
+ * k_cache, v_cache : [B, kv_num_heads, capacity, head_size] BNSH (appended)
+ * seqlens_k : device int32 [B]; sequence b holds total_b = seqlens_k[b] + 1
+ *           keys after this step.  The new rows go to cache rows
+ *           [past_b, past_b + k_seq) with past_b = total_b - k_seq; query row
+ *           s sits at position first_b + s with first_b = total_b - q_seq and
+ *           sees cache rows j <= first_b + s (the tail-aligned causal rule) and,
+ *           with local_window W > 0, only j >= first_b + s + 1 - W.
+ * rotary_dim : 0 = no rotary embedding; else even, 2 <= rotary_dim <=
+ *           head_size, and k_seq is 0 or q_seq.  cos_cache and sin_cache are
+ *           [cache_rows, rotary_dim / 2] of type rotary_dtype (PVA_F32, or
+ *           PVA_F16 when dtype is f16 or bf16).  Pair k < rotary_dim / 2 of a
+ *           head row is (2k, 2k+1) if rotary_interleaved, else (k, k +
+ *           rotary_dim/2); it is rotated by (c, s) = the tables' entry
+ *           [position][k] as (c x0 - s x1, s x0 + c x1) in f32, each product
+ *           and difference rounded on its own, then rounded to dtype; dims at
+ *           or past rotary_dim are copied.  position_ids (device int64
+ *           [B, q_seq], or NULL) gives the positions of the query rows and of
+ *           the appended rows; NULL means first_b + s and past_b + s.
+ *           Rotated queries go to library scratch; q itself is not written.
+ * out     : [B, q_seq, num_heads, head_size] (every row written).
+ * scale, softcap, dtype, stream : as pva_forward (v_head_size = head_size).
+ *
+ * Host errors (nothing enqueued): null pointers, B < 1, q_seq < 1, k_seq < 0,
+ * capacity < 1, (B + 1) * capacity or B * q_seq beyond int32, odd head_size,
+ * a bad rotary_dim / table / rotary_dtype, rotary with k_seq not in {0,
+ * q_seq}, plus pva_forward's checks (head sizes, alignment, dtype).
+ * Device errors: the step is all or nothing.  It is rejected if, for some b,
+ * total_b exceeds int32, past_b < 0, first_b < 0, past_b > capacity or
+ * total_b > capacity, or (rotary) a position lies outside [0, cache_rows) --
+ * the bounds the page's metadata kernel checks -- and also if
+ * PVA_DEV_KV_CACHE is already latched on the stream (a later step must not
+ * append after rows a rejected step skipped: read and clear the bit with
+ * pva_get_status, repair the cache, then go on).  A rejected step latches
+ * PVA_DEV_KV_CACHE and writes neither the cache nor `out`.
+ * Cache rows at or past total_b are never read (a sequence's last key tile
+ * is shifted back to end at its last key), so they may hold anything, NaN
+ * included.
+ * k_new/v_new must not overlap the cache rows being written.
+ */
+int pva_gqa_kvcache(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                    void* v_cache, const int32_t* seqlens_k, const void* cos_cache,
+                    const void* sin_cache, const int64_t* position_ids, void* out, int B,
+                    int q_seq, int k_seq, int capacity, int num_heads, int kv_num_heads,
+                    int head_size, int rotary_dim, int cache_rows, int rotary_interleaved,
+                    int rotary_dtype, float scale, float softcap, int local_window, int dtype,
+                    void* stream);
 
 /*
  * pva_forward_noalloc -- the same attention as pva_forward, for callers that
