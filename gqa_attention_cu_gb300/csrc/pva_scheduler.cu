@@ -16,7 +16,8 @@
 //   * zeroed split-completion counters for the decode combine, and zeroed
 //     work counters from which the persistent compute kernels draw items.
 //
-// One CTA of 128, 512 or 1024 threads (by B).  B <= 2048 sequences are sorted in shared memory
+// One warp for B <= 32 (everything in registers), else one CTA of 128, 512 or
+// 1024 threads (by B).  B <= 2048 sequences are sorted in shared memory
 // (bitonic); larger batches keep their input order.
 #include <limits.h>
 
@@ -318,6 +319,128 @@ __global__ void __launch_bounds__(NT) pva_schedule_kernel(AttnParams p, SchedCon
   }
 }
 
+// Warp-level sums (long long) over the 32 lanes.
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// The same scheduler for B <= 32, in one warp: sequence b lives in lane b,
+// the two lists are sorted with a bitonic network over the lanes (shuffles)
+// and their prefixes are warp scans.  Nothing goes through shared memory or
+// CTA barriers, which dominate the CTA version at small B; the work lists,
+// counters and status bits are identical.
+__global__ void __launch_bounds__(32) pva_schedule_warp_kernel(AttnParams p, SchedConfig c) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x, B = p.B;
+  const WsLayout L{B, p.Hkv};
+  int32_t* ws = p.ws;
+  const bool mine = lane < B;
+
+  uint32_t st = 0;
+  int lq = 0, lkv = 0;
+  if (mine) {
+    lq = p.cu_q[lane + 1] - p.cu_q[lane];
+    const int slot = p.cu_kv[lane + 1] - p.cu_kv[lane];
+    lkv = p.kv_len ? p.kv_len[lane] : slot;
+    if (lq < 0) st |= PVA_DEV_CU_Q_ORDER;
+    if (slot < 0) st |= PVA_DEV_CU_KV_ORDER;
+    if (lkv < 0 || lkv > slot) st |= p.kv_cap ? PVA_DEV_KV_CACHE : PVA_DEV_KV_LEN;
+  }
+  if (lane == 0) {
+    if (p.cu_q[0] != 0) st |= PVA_DEV_CU_Q_START;
+    if (p.cu_kv[0] != 0) st |= PVA_DEV_CU_KV_START;
+    if ((!p.q || !p.out) && p.cu_q[B] != 0) st |= PVA_DEV_NULL_TENSOR;
+    if ((!p.k || !p.v) && p.cu_kv[B] != 0) st |= PVA_DEV_NULL_TENSOR;
+  }
+  st = __reduce_or_sync(full, st);
+  int32_t* done = ws + L.dec_done();
+  for (int i = lane; i < B * p.Hkv; i += 32) done[i] = 0;
+  if (lane < 4) ws[L.counters() + lane] = 0;
+
+  int n_pref = 0, n_items = 0, n_dec = 0, n_units = 0, chunk = INT_MAX;
+  if (st == 0) {
+    const bool is_dec = mine && c.decode_enabled && lq == 1;
+    if (c.decode_enabled) {
+      const long long keyrows = warp_sum_ll(is_dec ? decode_keys(lkv, p.window) : 0) * p.Hkv;
+      const long long target = (long long)c.num_sms * 8;
+      long long ch = (keyrows + target - 1) / target;
+      ch = ((ch + 63) / 64) * 64;
+      if (ch < 256) ch = 256;
+      for (int it = 0; it < 40; ++it) {
+        const int sp =
+            is_dec ? decode_splits(decode_keys(lkv, p.window), ch > INT_MAX ? INT_MAX : (int)ch)
+                   : 0;
+        const long long units = warp_sum_ll((long long)sp * p.Hkv);
+        if (!__any_sync(full, sp > 1) || units <= p.dec_cap_units) break;
+        ch *= 2;
+      }
+      chunk = ch > INT_MAX ? INT_MAX : (int)ch;
+    }
+    bool ok = true;
+#pragma unroll 1
+    for (int cls = 0; cls < 2; ++cls) {
+      const bool member = mine && lq > 0 && (cls == 1 ? is_dec : !is_dec);
+      unsigned long long key =
+          member ? ((unsigned long long)(unsigned)(INT_MAX - lkv) << 32) | (unsigned)lane : ~0ull;
+#pragma unroll
+      for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+          const unsigned long long other = __shfl_xor_sync(full, key, j);
+          const unsigned long long lo = key < other ? key : other, hi = key < other ? other : key;
+          key = (((lane & j) == 0) == ((lane & k) == 0)) ? lo : hi;
+        }
+      const int n = __popc(__ballot_sync(full, member));
+      const int o = key != ~0ull ? (int)(key & 0xffffffffu) : -1;
+      int32_t* order = ws + (cls == 0 ? L.pref_order() : L.dec_order());
+      int32_t* prefix = ws + (cls == 0 ? L.pref_prefix() : L.dec_prefix());
+      if (mine) order[lane] = o;
+      const int lq_o = __shfl_sync(full, lq, o & 31), lkv_o = __shfl_sync(full, lkv, o & 31);
+      long long w = 0;
+      if (lane < n)
+        w = cls == 0 ? (long long)((lq_o + c.tile_tokens - 1) / c.tile_tokens) * c.units_per_tile
+                     : (long long)decode_splits(decode_keys(lkv_o, p.window), chunk) * p.Hkv;
+      long long incl = w;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const long long y = __shfl_up_sync(full, incl, d);
+        if (lane >= d) incl += y;
+      }
+      const long long total = __shfl_sync(full, incl, 31);
+      const bool fits = total <= (long long)INT_MAX;
+      if (fits) {
+        if (lane < n) prefix[lane] = (int32_t)(incl - w);
+        for (int i = n + lane; i <= B; i += 32) prefix[i] = (int32_t)total;
+      }
+      ok = ok && fits;
+      if (cls == 0) {
+        n_pref = n;
+        n_items = fits ? (int)total : 0;
+      } else {
+        n_dec = n;
+        n_units = fits ? (int)total : 0;
+      }
+    }
+    if (!ok) st |= PVA_DEV_TOO_MANY;
+  }
+  if (lane == 0) {
+    SchedHeader h;
+    h.status = st;
+    h.n_pref = st ? 0 : n_pref;
+    h.n_items = st ? 0 : n_items;
+    h.n_dec = st ? 0 : n_dec;
+    h.n_units = st ? 0 : n_units;
+    h.tile_tokens = c.tile_tokens;
+    h.units_per_tile = c.units_per_tile;
+    h.dec_chunk = st ? 0 : chunk;
+    *reinterpret_cast<SchedHeader*>(ws + kWsHeader) = h;
+    if (st) atomicOr(p.status, st);
+  }
+}
+
 }  // namespace
 
 // Front end of pva_forward_padded: the padded layout as packed offsets.  Batch
@@ -348,7 +471,9 @@ cudaError_t launch_padded_front(const int64_t* nonpad, int B, int q_seq, int kv_
 }
 
 cudaError_t launch_scheduler(const AttnParams& p, const SchedConfig& c, cudaStream_t s) {
-  if (p.B <= 128)
+  if (p.B <= 32)
+    pva_schedule_warp_kernel<<<1, 32, 0, s>>>(p, c);
+  else if (p.B <= 128)
     pva_schedule_kernel<128><<<1, 128, 0, s>>>(p, c);
   else if (p.B <= 512)
     pva_schedule_kernel<512><<<1, 512, 0, s>>>(p, c);

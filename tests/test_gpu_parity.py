@@ -402,6 +402,25 @@ def test_scheduler_matches_host_mirror(seed, cfg):
     assert words == sched_mirror(lq, lkv, H, Hkv, d, dtype, sms, dv)
 
 
+@pytest.mark.parametrize("B", [1, 2, 7, 31, 32, 33])
+@pytest.mark.parametrize("cfg", [(32, 8, 128, 128, 2), (8, 1, 256, 256, 2), (4, 4, 64, 64, 0),
+                                 (16, 4, 192, 128, 2)])
+def test_scheduler_small_batches_match_host_mirror(B, cfg):
+    """B <= 32 runs the one-warp scheduler (33 the CTA one): same words."""
+    H, Hkv, d, dv, dtype = cfg
+    g = torch.Generator().manual_seed(B)
+    lq = torch.randint(0, 400, (B,), generator=g)
+    r = torch.rand(B, generator=g)
+    lq = torch.where(r < 0.35, torch.ones_like(lq), torch.where(r > 0.9, torch.zeros_like(lq), lq))
+    lq = lq.tolist()
+    lkv = (torch.tensor(lq) + torch.randint(0, 20000, (B,), generator=g)).tolist()
+    dev = torch.device("cuda:0")
+    words = pva.pva_schedule(workloads.cu_from_lengths(lq).to(dev),
+                             workloads.cu_from_lengths(lkv).to(dev), B, H, Hkv, d, dv, 1, dtype)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert words == sched_mirror(lq, lkv, H, Hkv, d, dtype, sms, dv)
+
+
 def test_scheduler_configs_match_host_mirror():
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     dev = torch.device("cuda:0")
