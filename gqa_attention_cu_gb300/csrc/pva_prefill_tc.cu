@@ -26,7 +26,7 @@
 //               after that MMA (tcgen05 MMAs of one thread run in issue order).
 //   warps 2..5  softmax / correction / epilogue, one thread per TMEM lane.
 // TMEM: S buffers [0,64) and [64,128), O [128,128+dv).  Shared memory (d = dv
-// = 256): Q 64 KB + 5 K/V slots of 32 KB.
+// = 256): Q 64 KB + 5 K/V slots of 32 KB (more, smaller slots at d < 256).
 //
 // Softcap: tanh(t) of the scaled score t = s * scale / softcap comes from its
 // Maclaurin series t - t^3/3 + 2t^5/15 - 17t^7/315 + 62t^9/2835 -
@@ -58,7 +58,12 @@ struct TcCfg {
   static constexpr int K_BYTES = KCH * KV_CHUNK;
   static constexpr int V_BYTES = VCH * KV_CHUNK;
   static constexpr int KV_TILE = K_BYTES > V_BYTES ? K_BYTES : V_BYTES;  // one ring slot
-  static constexpr int SLOTS = 5;
+  // As many K/V slots as shared memory holds next to Q (at most 8): 5 at
+  // d = 256, 7 at d = 192, 8 at d = 96.  A deeper ring starts each load
+  // earlier before its tile is needed.
+  static constexpr int SLOTS_FIT = (232448 - 64 - 2048 - Q_BYTES) / KV_TILE;
+  static constexpr int SLOTS = SLOTS_FIT < 8 ? SLOTS_FIT : 8;
+  static_assert(SLOTS >= 4, "K/V ring depth");
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = Q_BYTES;
   static constexpr int OFF_BAR = OFF_RING + SLOTS * KV_TILE;
@@ -350,10 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n <= 2) commit(&bars->q_empty);
       for (int j = 0; ok && j < n; ++j) {
         const uint32_t T_ = gt + j, Lv = loads + 2 * j + 1;
-        // V_j and K_{j+2} have normally landed before P(j) is ready: wait for
-        // them first, so that only the issue follows the P(j) arrival.
+        // P.V(j) needs V_j and P(j) only.  K_{j+2} is waited for only after
+        // P.V(j) is issued: its ring slot is the one used SLOTS loads before,
+        // so its load starts late, and waiting for it first would hold P.V(j)
+        // -- and with it the slot of the load after -- behind a load latency.
         if (!(ok = wait_slot(Lv))) break;
-        if (j + 2 < n && !(ok = wait_slot(loads + 2 * (j + 2)))) break;
         if (j == 0 && !(ok = wait(&bars->o_free, (items & 1) ^ 1))) break;
         if (!(ok = wait(&bars->p_full[T_ & 1], (T_ >> 1) & 1))) break;
         tc_fence_after();
@@ -370,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&bars->ring_empty[Lv % C::SLOTS]);
         }
         if (j + 2 < n) {
+          if (!(ok = wait_slot(loads + 2 * (j + 2)))) break;
           issue_s(T_ + 2, loads + 2 * (j + 2));
           if (j + 3 == n) commit(&bars->q_empty);
         }
