@@ -115,16 +115,20 @@ __device__ __forceinline__ void extremes64(const uint32_t (&va)[32], const uint3
   mn = fminf(b[0], b[1]);
 }
 
-// Maclaurin series of tanh through t^11 (|t| <= 1/2).
-__device__ __forceinline__ float tanh_series(float t) {
-  const float u = t * t;
-  float p = -0.008863235529902197f;
-  p = fmaf(p, u, 0.021869488536155203f);
-  p = fmaf(p, u, -0.05396825396825397f);
-  p = fmaf(p, u, 0.13333333333333333f);
-  p = fmaf(p, u, -0.3333333333333333f);
-  p = fmaf(p, u, 1.0f);
-  return t * p;
+// tanh(t) for |t| <= 1/2 from its Maclaurin series through t^11 (Horner in
+// t^2; truncation error below 4e-7), on a pair of scores with packed f32x2
+// FMAs (a product is an FMA with a zero addend): half the instructions of
+// the scalar chain, the same rounded operations in each lane.
+__device__ __forceinline__ float2 tanh_series2(float2 t) {
+  const float2 z = make_float2(0.0f, 0.0f);
+  const float2 u = ffma2(t, t, z);
+  float2 p = make_float2(-0.008863235529902197f, -0.008863235529902197f);
+  p = ffma2(p, u, make_float2(0.021869488536155203f, 0.021869488536155203f));
+  p = ffma2(p, u, make_float2(-0.05396825396825397f, -0.05396825396825397f));
+  p = ffma2(p, u, make_float2(0.13333333333333333f, 0.13333333333333333f));
+  p = ffma2(p, u, make_float2(-0.3333333333333333f, -0.3333333333333333f));
+  p = ffma2(p, u, make_float2(1.0f, 1.0f));
+  return ffma2(t, p, z);
 }
 
 // 2^(x - m) over the 64 columns, row sum, P packed as 16-bit pairs.
@@ -142,8 +146,8 @@ __device__ __forceinline__ float exp64(const uint32_t (&va)[32], const uint32_t 
     if (MODE == 0) {
       x = ffma2(s, mul2, neg_m);
     } else if (MODE == 1) {
-      x.x = fmaf(cap_mul, tanh_series(s.x * s_mul), -m_eff);
-      x.y = fmaf(cap_mul, tanh_series(s.y * s_mul), -m_eff);
+      const float2 z = make_float2(0.0f, 0.0f), cap2 = make_float2(cap_mul, cap_mul);
+      x = ffma2(cap2, tanh_series2(ffma2(s, mul2, z)), neg_m);
     } else {
       x.x = fmaf(cap_mul, tanh_via_exp2(s.x * s_mul), -m_eff);
       x.y = fmaf(cap_mul, tanh_via_exp2(s.y * s_mul), -m_eff);
