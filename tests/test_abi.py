@@ -100,3 +100,34 @@ def test_padded_host_argument_checks_need_no_gpu(lib, kw, code):
     kv_seq, B * q_seq and B * kv_seq within int32)."""
     assert _call_padded(lib, **kw) == code
     assert pva.pva_last_error() != ""
+
+
+def _call_kvcache(lib, **kw):
+    args = dict(q=16, kn=16, vn=16, kc=16, vc=16, sk=16, cos=16, sin=16, pid=None, out=16, B=2,
+                q_seq=1, k_seq=1, cap=64, H=8, Hkv=2, d=128, rot=0, rows=0, inter=0,
+                rot_dtype=0, scale=0.0, softcap=0.0, window=0, dtype=2)
+    args.update(kw)
+    a = args
+    return lib.pva_gqa_kvcache(a["q"], a["kn"], a["vn"], a["kc"], a["vc"], a["sk"], a["cos"],
+                               a["sin"], a["pid"], a["out"], a["B"], a["q_seq"], a["k_seq"],
+                               a["cap"], a["H"], a["Hkv"], a["d"], a["rot"], a["rows"],
+                               a["inter"], a["rot_dtype"], a["scale"], a["softcap"],
+                               a["window"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(kc=None), -1), (dict(sk=None), -1), (dict(out=None), -1),
+    (dict(B=0), -1), (dict(q_seq=0), -1), (dict(k_seq=-1), -1), (dict(cap=0), -1),
+    (dict(kn=None), -1), (dict(B=3, cap=1 << 29), -1),
+    (dict(d=127), -2),
+    (dict(rot=3, rows=8), -1), (dict(rot=256, rows=8), -1), (dict(rot=64, rows=0), -1),
+    (dict(rot=64, rows=8, cos=None), -1), (dict(rot=64, rows=8, q_seq=4, k_seq=2), -1),
+    (dict(rot=64, rows=8, rot_dtype=2), -1), (dict(rot=64, rows=8, rot_dtype=1, dtype=0), -1),
+    (dict(H=6, Hkv=4), -1), (dict(dtype=5), -1),
+])
+def test_kvcache_host_argument_checks_need_no_gpu(lib, kw, code):
+    """pva_gqa_kvcache rejects malformed calls on the host, before any CUDA
+    call: null pointers, counts, the cache extent, odd head sizes, rotary
+    dimensions and tables, rotary with k_seq not in {0, q_seq}, table types."""
+    assert _call_kvcache(lib, **kw) == code
+    assert pva.pva_last_error() != ""
