@@ -254,12 +254,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Items are drawn from a device-wide counter (zeroed by the scheduler):
       // a CTA takes the next item of the longest-first list when it is ready
       // for one, which balances uneven item costs across the persistent grid.
-      // The next index is taken as soon as the current item is decoded, so
-      // the atomic's round trip overlaps the current item's loads.
+      // The next index is taken as soon as the current item starts, and the
+      // next item is decoded (a few dependent reads of the scheduler's lists)
+      // once the current item's first loads are out, so both latencies
+      // overlap the current item instead of delaying the next publish.
       int* next_item = p.ws + WsLayout{p.B, p.Hkv}.counters();
-      for (int idx = atomicAdd(next_item, 1), idx_next; ok && idx < h.n_items; idx = idx_next) {
-        const PrefillItem it = decode_prefill_item(p, h, idx);
-        idx_next = idx + 1 < h.n_items ? atomicAdd(next_item, 1) : h.n_items;
+      int idx = atomicAdd(next_item, 1);
+      PrefillItem it{};
+      if (idx < h.n_items) it = decode_prefill_item(p, h, idx);
+      while (ok && idx < h.n_items) {
+        const int idx_next = idx + 1 < h.n_items ? atomicAdd(next_item, 1) : h.n_items;
+        PrefillItem it_next = it;
+        bool decoded = idx_next >= h.n_items;
         const int hi = item_key_extent(it, h.tile_tokens, p.is_causal);
         ItemSlot v;
         v.q_start = it.q_start;
@@ -273,35 +279,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         v.q0 = min(it.q_start + it.t * h.tile_tokens, total_q - 2 * m_tok);
         v.last = 0;
         if (!(ok = publish(v))) break;
-        if (v.n_tiles == 0) continue;
-        const int g = v.unit;
-        if (!(ok = mbar_wait(&bars->q_empty, (items & 1) ^ 1, abort, status))) break;
-        mbar_arrive_expect_tx(&bars->q_full, q_bytes);
+        if (v.n_tiles > 0) {
+          const int g = v.unit;
+          if (!(ok = mbar_wait(&bars->q_empty, (items & 1) ^ 1, abort, status))) break;
+          mbar_arrive_expect_tx(&bars->q_full, q_bytes);
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-          for (int c = 0; c < C::KCH; ++c)
-            tma_load_3d(smem + C::OFF_Q + t * C::Q_TILE + c * C::Q_CHUNK, &tmap_q, &bars->q_full,
-                        c * 64, g * G, v.q0 + t * m_tok);
-        ++items;
-        for (int j = 0; ok && j < v.n_tiles; ++j) {
-          const int k0 = min(v.kv_start + (v.jb + j) * BN,
-                             key_tile_limit(p, v.kv_start, v.lkv, total_kv) - BN);
-          const int2 yz = kv_tma_yz(p, it.b, g, v.kv_start, k0);
-#pragma unroll
-          for (int kv = 0; kv < 2; ++kv, ++loads) {
-            const int sl = loads % C::SLOTS;
-            if (!(ok = mbar_wait(&bars->ring_empty[sl], ((loads / C::SLOTS) & 1) ^ 1, abort,
-                                 status)))
-              break;
-            uint8_t* dst = smem + C::OFF_RING + sl * C::KV_TILE;
-            mbar_arrive_expect_tx(&bars->ring_full[sl], (uint32_t)C::KV_TILE);
+          for (int t = 0; t < 2; ++t)
 #pragma unroll
             for (int c = 0; c < C::KCH; ++c)
-              tma_load_3d(dst + c * C::KV_CHUNK, kv ? &tmap_v : &tmap_k, &bars->ring_full[sl],
-                          c * 64, yz.x, yz.y);
+              tma_load_3d(smem + C::OFF_Q + t * C::Q_TILE + c * C::Q_CHUNK, &tmap_q,
+                          &bars->q_full, c * 64, g * G, v.q0 + t * m_tok);
+          ++items;
+          for (int j = 0; ok && j < v.n_tiles; ++j) {
+            const int k0 = min(v.kv_start + (v.jb + j) * BN,
+                               key_tile_limit(p, v.kv_start, v.lkv, total_kv) - BN);
+            const int2 yz = kv_tma_yz(p, it.b, g, v.kv_start, k0);
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv, ++loads) {
+              const int sl = loads % C::SLOTS;
+              if (!(ok = mbar_wait(&bars->ring_empty[sl], ((loads / C::SLOTS) & 1) ^ 1, abort,
+                                   status)))
+                break;
+              uint8_t* dst = smem + C::OFF_RING + sl * C::KV_TILE;
+              mbar_arrive_expect_tx(&bars->ring_full[sl], (uint32_t)C::KV_TILE);
+#pragma unroll
+              for (int c = 0; c < C::KCH; ++c)
+                tma_load_3d(dst + c * C::KV_CHUNK, kv ? &tmap_v : &tmap_k, &bars->ring_full[sl],
+                            c * 64, yz.x, yz.y);
+            }
+            if (!decoded) {
+              it_next = decode_prefill_item(p, h, idx_next);
+              decoded = true;
+            }
           }
         }
+        if (!ok) break;
+        if (!decoded) it_next = decode_prefill_item(p, h, idx_next);
+        idx = idx_next;
+        it = it_next;
       }
       if (ok) {
         ItemSlot v{};
