@@ -208,9 +208,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // Units are drawn from a device-wide counter (zeroed by the scheduler),
       // so CTAs that finish early take the next unit of the longest-first list.
+      // The next index is drawn when a unit starts and decoded (a binary
+      // search over the scheduler's prefix sums) right after the unit's first
+      // tile is requested, so neither latency sits between two units' loads.
       int* next_unit = p.ws + WsLayout{p.B, p.Hkv}.counters() + 1;
-      for (int u = atomicAdd(next_unit, 1); ok && u < h.n_units; u = atomicAdd(next_unit, 1)) {
-        Unit un = decode_unit(p, h, u);
+      int u = atomicAdd(next_unit, 1);
+      Unit un{};
+      if (u < h.n_units) un = decode_unit(p, h, u);
+      while (ok && u < h.n_units) {
+        const int u_next = atomicAdd(next_unit, 1);
+        Unit nx = un;
+        bool decoded = u_next >= h.n_units;
         un.u = u;
         un.last = 0;
         if (!(ok = publish(un))) break;
@@ -224,7 +232,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int2 yz = kv_tma_yz(p, un.b, un.g, un.kv_start, k0);
           tma_load_3d(dk, &tmap_k, &full[st], 0, yz.x, yz.y);
           tma_load_3d(dk + C::TILE_BYTES, &tmap_v, &full[st], 0, yz.x, yz.y);
+          if (!decoded) {
+            nx = decode_unit(p, h, u_next);
+            decoded = true;
+          }
         }
+        if (!ok) break;
+        if (!decoded) nx = decode_unit(p, h, u_next);
+        u = u_next;
+        un = nx;
       }
       if (ok) {
         Unit v{};
