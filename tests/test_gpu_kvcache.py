@@ -196,3 +196,24 @@ def test_other_bounds_reject_the_step(case):
                         to(sin))
     assert pva.pva_get_status() == pva.DEV_FLAGS["kv_cache"]
     assert same_bits(kcd.cpu(), kc) and torch.isnan(out.float()).all()
+
+
+def test_full_size_step_sampled_sequences():
+    """The step the benchmark times (B = 256, capacity 8192, totals up to
+    8192, rotary on 128 dims), checked on sampled sequences: their appended
+    cache rows bit for bit and their outputs within the bf16 tolerance."""
+    from gqa_attention_cu_gb300 import workloads
+    c = workloads.make_cache_step("bf16_kvcache_decode", seed=0, device="cuda:0")
+    B, H, Hkv, d = c["B"], c["num_heads"], c["kv_num_heads"], c["head_size"]
+    pick = [0, 1, B // 2, B - 1]
+    k0, v0 = c["k_cache"][pick].cpu(), c["v_cache"][pick].cpu()
+    out = torch.empty_like(c["q"])
+    pva.pva_gqa_kvcache(c["q"], c["k_new"], c["v_new"], c["k_cache"], c["v_cache"],
+                        c["seqlens_k"], out, H, Hkv, c["cos"], c["sin"])
+    assert pva.pva_get_status() == 0
+    ref, ka, va, bits = gqa_cache.gqa_cache_step(
+        c["q"][pick].cpu(), c["k_new"][pick].cpu(), c["v_new"][pick].cpu(), k0, v0,
+        c["seqlens_k"][pick].cpu().tolist(), H, Hkv, c["cos"].cpu(), c["sin"].cpu())
+    assert bits == 0
+    assert same_bits(c["k_cache"][pick].cpu(), ka) and same_bits(c["v_cache"][pick].cpu(), va)
+    check(out[pick].reshape(-1, H, d), ref.reshape(-1, H, d), "bf16")
