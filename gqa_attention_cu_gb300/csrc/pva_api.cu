@@ -11,6 +11,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <string>
@@ -67,7 +68,10 @@ struct Workspace {
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_dev;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+// Resolved once per process; every entry point (whichever lock it holds)
+// goes through get_encoder, so the lookup is guarded by its own once-flag.
+std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
+std::once_flag g_encode_once;
 
 int device_info(int dev, DeviceInfo* out) {
   auto& d = g_dev[dev];
@@ -81,14 +85,16 @@ int device_info(int dev, DeviceInfo* out) {
 }
 
 int get_encoder() {
-  if (g_encode) return PVA_OK;
-  cudaDriverEntryPointQueryResult q;
-  void* fn = nullptr;
-  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                   cudaEnableDefault, &q);
-  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess && fn)
+      g_encode.store(reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn));
+  });
+  if (!g_encode.load())
     return fail(PVA_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
-  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   return PVA_OK;
 }
 
@@ -102,12 +108,13 @@ int encode_map(CUtensorMap* map, const void* base, int dtype, int dim, int heads
   const cuuint64_t gstride[2] = {(cuuint64_t)dim * 2, (cuuint64_t)dim * heads * 2};
   const cuuint32_t box[3] = {(cuuint32_t)box_dim, (cuuint32_t)box_heads, (cuuint32_t)box_tokens};
   const cuuint32_t estride[3] = {1, 1, 1};
-  CUresult r = g_encode(map, dtype == PVA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                        3, const_cast<void*>(base), gdim, gstride, box, estride,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const auto encode = g_encode.load();
+  CUresult r = encode(map, dtype == PVA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                      3, const_cast<void*>(base), gdim, gstride, box, estride,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char msg[160];
     snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled failed (%d) dim=%d heads=%d box=%dx%dx%d",
@@ -126,12 +133,13 @@ int encode_plane_map(CUtensorMap* map, const void* base, int dtype, int dim, int
   const cuuint64_t gstride[2] = {(cuuint64_t)dim * 2, (cuuint64_t)dim * rows * 2};
   const cuuint32_t box[3] = {(cuuint32_t)box_dim, (cuuint32_t)box_rows, 1};
   const cuuint32_t estride[3] = {1, 1, 1};
-  CUresult r = g_encode(map, dtype == PVA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                        3, const_cast<void*>(base), gdim, gstride, box, estride,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const auto encode = g_encode.load();
+  CUresult r = encode(map, dtype == PVA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                      3, const_cast<void*>(base), gdim, gstride, box, estride,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char msg[160];
     snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled failed (%d) dim=%d rows=%d planes=%lld",
@@ -637,6 +645,7 @@ void pva_release(void) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return;
   cudaDeviceSynchronize();
+  noalloc_forget_device(dev);
   for (auto it = g_ws.begin(); it != g_ws.end();) {
     if (it->first.first == dev) {
       if (it->second.buf) cudaFree(it->second.buf);

@@ -126,6 +126,9 @@ int cuda_fail(cudaError_t e, const char* what);
 int get_encoder();
 int encode_map(CUtensorMap* map, const void* base, int dtype, int dim, int heads, int box_dim,
                int box_heads, int box_tokens, bool swizzle128);
+// Drops pva_forward_noalloc's cached address of its static scratch on `dev`
+// (the next call looks it up again in the current context).
+void noalloc_forget_device(int dev);
 int check_and_plan(const void* q, const void* k, const void* v, const int32_t* cu_q,
                    const int32_t* cu_kv, void* out, int B, int H, int Hkv, int d, int dv,
                    float scale, float softcap, int dtype, Plan* plan);

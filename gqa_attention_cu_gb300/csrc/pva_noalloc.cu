@@ -7,8 +7,10 @@
 // first use; this entry point never calls cudaMalloc, cudaFree or any
 // allocating library routine.  Its scratch (the scheduler's work lists, the
 // decode kernel's split partials and completion counters, and a status word)
-// lives in one file-scope device array of fixed size, so every GPU that loads
-// the library holds those 4 MiB until the process exits.
+// lives in one file-scope device array of fixed size.  The array belongs to
+// the library's device code: on each device it is bound when that code is
+// loaded there (with CUDA's lazy module loading, at the first call that needs
+// it) and those 4 MiB stay taken until the process exits.
 //
 // Consequences for callers:
 //   * Every call on a device shares the one array.  Calls whose kernels
@@ -24,9 +26,16 @@
 //     PVA_ERR_UNSUPPORTED; decode split partials are limited to what fits in
 //     the rest of the array (the scheduler picks fewer, larger splits when
 //     needed).
+//   * Without a caller status word the call latches its device-side errors
+//     (malformed offsets, NULL tensors with a nonzero extent, a pipeline wait
+//     that gave up) into a word inside the array that nothing reads back:
+//     such a call leaves the output unwritten and the caller is not told.
+//     Pass a status word to learn of them.
 //   * The first call on each device resolves the array's device address
 //     (cudaGetSymbolAddress, with that device current) and caches it; make that
-//     first call before any stream capture.
+//     first call before any stream capture.  The address belongs to the
+//     context current at that call: after a device reset call pva_release (it
+//     drops the cached address) before calling again.
 #include <math.h>
 
 #include <mutex>
@@ -71,6 +80,15 @@ int device_scratch(int dev, DeviceScratch* out) {
 }
 
 }  // namespace
+
+namespace pva {
+namespace host {
+void noalloc_forget_device(int dev) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (dev >= 0 && dev < kMaxDevices) g_dev[dev] = DeviceScratch{};
+}
+}  // namespace host
+}  // namespace pva
 
 extern "C" int pva_forward_noalloc(const void* q, const void* k, const void* v,
                                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,

@@ -223,11 +223,16 @@ int pva_gqa_kvcache(const void* q, const void* k_new, const void* v_new, void* k
  *
  * It calls no cudaMalloc, cudaFree or allocating library routine: its scratch
  * (work lists, decode split partials and counters, a status word) is one
- * file-scope device array of 4 MiB that every GPU loading the library holds
- * until the process exits.  Arguments are those of pva_forward, plus:
+ * file-scope device array of 4 MiB.  A device holds it from the moment the
+ * library's device code is loaded there (with CUDA's lazy module loading: the
+ * first call that needs that code) until the process exits.  Arguments are
+ * those of pva_forward, plus:
  *   device_status : optional device pointer to a uint32 the call ORs its
- *                   PVA_DEV_* bits into (the caller clears it); NULL uses a
- *                   word inside the scratch, which each call clears first.
+ *                   PVA_DEV_* bits into (the caller clears it).  NULL uses a
+ *                   word inside the scratch, which each call clears first and
+ *                   nothing reads back: device-side errors (malformed offsets,
+ *                   NULL tensors with a nonzero extent, a wait that gave up)
+ *                   then leave `out` unwritten without telling the caller.
  * Limits: B * (4 + kv_num_heads) int32 words of work lists must fit in 1 MiB
  * (else PVA_ERR_UNSUPPORTED with nothing enqueued); decode splits are limited
  * to the partials that fit in the rest of the array.  All calls on a device
@@ -235,8 +240,9 @@ int pva_gqa_kvcache(const void* q, const void* k_new, const void* v_new, void* k
  * results, so keep them ordered (one stream, or events between streams).  The
  * array keeps the last call's contents; what must start at zero is cleared
  * by each call.  The first call on each device looks up the array's device
- * address (cudaGetSymbolAddress with that device current); make it before any
- * stream capture.
+ * address (cudaGetSymbolAddress with that device current) and caches it; make
+ * it before any stream capture.  The cached address belongs to the context of
+ * that call: after a device reset, call pva_release (which drops it) first.
  */
 int pva_forward_noalloc(const void* q, const void* k, const void* v,
                         const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
@@ -306,7 +312,8 @@ const char* pva_status_string(int code);
 const char* pva_last_error(void);
 
 /* Frees every workspace the library holds on the current device (waits for
- * the streams that used them first). */
+ * the streams that used them first), and drops pva_forward_noalloc's cached
+ * address of its static scratch on that device. */
 void pva_release(void);
 
 /* Library version as (major << 16) | (minor << 8) | patch. */
