@@ -9,9 +9,14 @@ FLOPs each, 4*H*d when d == dv).  The decode workload reports KV-read GB/s inste
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl reference]
 
-Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
-oracle (the only reference this build has) on a bounded sample of the same
-workload.  Under torchrun every rank runs its own batch (seed = rank): the
+Prints ONE JSON line (rank 0).  Besides the cold-L2 headline it carries the
+same steps with a warm L2 (``warm_l2``), median and minimum step times, and,
+for the default workload on one GPU, the other configs each in its own timed
+region (``other_configs``: chunked prefill, decode, long-context MQA with
+softcap).  ``cpu_baseline`` times the fp64 oracle on the host cores (all of
+them and one) and, for the default line, checks the fp32 workload against it.
+``--impl reference`` times the fp64 CPU oracle (the only reference this
+build has) on a bounded sample of the same workload.  Under torchrun every rank runs its own batch (seed = rank): the
 work is independent per GPU (weak scaling, no data-path collective).
 """
 from __future__ import annotations
@@ -205,12 +210,13 @@ class OracleSampler:
     rows.  Work is counted like the GPU arm's (visible pairs x 4 d FLOPs, or
     K/V bytes for decode)."""
 
-    def __init__(self, w_name: str, seed: int = 0):
+    def __init__(self, w_name: str, seed: int = 0, threads: int = 0):
         import numpy as np
         import torch
 
         from gqa_attention_cu_gb300 import workloads
         self.np, self.torch, self.wl = np, torch, workloads
+        self.threads = threads  # 0: every host core (OpenMP default)
         self.name = w_name
         self.spec = workloads.WORKLOADS[w_name]
         gen = torch.Generator("cpu").manual_seed(seed)
@@ -235,7 +241,7 @@ class OracleSampler:
         pairs = int(vis[rows // H].sum())
         t0 = time.perf_counter()
         oracle.attention_rows(q, k, v, cq, ck, rows, H, Hkv, sp.scale, sp.is_causal, sp.softcap,
-                              local_window=sp.window)
+                              threads=self.threads, local_window=sp.window)
         return time.perf_counter() - t0, pairs, n_rows
 
     def run(self, seconds: float):
@@ -308,8 +314,30 @@ class CacheStepSampler:
         return kv_bytes / secs / 1e9, "GB/s"
 
 
-def make_sampler(w_name: str):
-    return CacheStepSampler(w_name) if w_name == "bf16_kvcache_decode" else OracleSampler(w_name)
+def make_sampler(w_name: str, threads: int = 0):
+    if w_name == "bf16_kvcache_decode":
+        return CacheStepSampler(w_name)
+    return OracleSampler(w_name, threads=threads)
+
+
+def cpu_model() -> str:
+    """Host CPU model (lscpu, else /proc/cpuinfo), for the baseline record."""
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for ln in r.stdout.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 def run_reference(args, w_name):
@@ -346,8 +374,9 @@ def run_reference(args, w_name):
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(w_name, seconds=12.0):
-    """The oracle as it stands on the host cores, on a bounded sample."""
+def cpu_baseline(w_name, seconds=12.0, single_thread_seconds=4.0):
+    """The oracle as it stands on the host cores, on a bounded sample, plus a
+    shorter single-thread sample of the same recipe."""
     import oracle
     smp = make_sampler(w_name)
     secs, pairs, rows = smp.run(seconds)
@@ -355,8 +384,39 @@ def cpu_baseline(w_name, seconds=12.0):
     what = ("sequences of the workload's length draw, whole cache step each"
             if w_name == "bf16_kvcache_decode" else
             "random (token, head) output rows from sequences of the workload's length draw")
-    return {"value": value, "unit": unit, "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"{rows} {what}, {secs:.1f} s"}
+    rec = {"value": value, "unit": unit, "cores": oracle.max_threads(), "kind": "oracle",
+           "cpu_model": cpu_model(), "sample": f"{rows} {what}, {secs:.1f} s"}
+    if w_name != "bf16_kvcache_decode" and single_thread_seconds > 0:
+        one = make_sampler(w_name, threads=1)
+        s1, p1, r1 = one.run(single_thread_seconds)
+        v1, _ = one.value(s1, p1)
+        rec["single_thread"] = {"value": v1, "unit": unit, "cores": 1,
+                                "sample": f"{r1} {what}, {s1:.1f} s"}
+    return rec
+
+
+def fp32_oracle_check(pva, dev):
+    """The fp32_small workload through pva_forward, against the fp64 oracle
+    (which is timed too): the accuracy figure of the fp32 path."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from gqa_attention_cu_gb300 import workloads
+    w = workloads.make("fp32_small")
+    args = [w[k_].to(dev) for k_ in ("q", "k", "v", "cu_q", "cu_kv")]
+    out = torch.empty(w["q"].shape[0], w["num_heads"], w["v_head_size"], dtype=torch.float32,
+                      device=dev)
+    pva.pva_forward(*args, out, w["B"], w["num_heads"], w["kv_num_heads"], w["head_size"],
+                    w["v_head_size"], w["scale"], int(w["is_causal"]), w["softcap"])
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    ref = oracle.attention(w["q"], w["k"], w["v"], w["cu_q"], w["cu_kv"], w["num_heads"],
+                           w["kv_num_heads"], w["scale"], w["is_causal"], w["softcap"])
+    t_oracle = time.perf_counter() - t0
+    err = np.abs(out.double().cpu().numpy() - ref)
+    return {"max_abs_vs_oracle": float(err.max()), "tolerance": 2e-5,
+            "oracle_ms_full": 1e3 * t_oracle}
 
 
 def bench_kvcache(args, rank, world, local, dev):
@@ -481,6 +541,132 @@ def bench_kvcache(args, rank, world, local, dev):
         torch.distributed.destroy_process_group()
 
 
+def dominant_kernel(w):
+    if w["dtype"] == "f32":
+        return "pva_prefill_f32_kernel"
+    if w["head_size"] == w["v_head_size"] and w["head_size"] in (64, 128):
+        return "pva_prefill_pair_kernel"
+    return "pva_prefill_tc_kernel"
+
+
+def launches_per_step(w):
+    """Kernels one pva_forward launches: scheduler, prefill, and the split-KV
+    decode kernel for the shapes it serves."""
+    G = w["num_heads"] // w["kv_num_heads"]
+    dec = (w["dtype"] != "f32" and G in (1, 2, 4, 8) and w["head_size"] == w["v_head_size"]
+           and w["head_size"] in (64, 128, 256))
+    return 3 if dec else 2
+
+
+def time_steps(pva, forward, stream, dev, steps, flush):
+    """`steps` device-timed calls (CUDA events on the launching stream); with
+    `flush` a 256 MB buffer is written between calls (cold L2).  Returns the
+    per-step times and the per-kernel times of each call."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    kernel_ms = []
+    torch.cuda.synchronize(dev)
+    pva.pva_profile(True)
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            if flush is not None:
+                flush.fill_(i & 0xff)
+            starts[i].record(stream)
+            forward(stream)
+            ends[i].record(stream)
+            kernel_ms.append(pva.pva_kernel_times())
+    torch.cuda.synchronize(dev)
+    pva.pva_profile(False)
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], kernel_ms
+
+
+def step_stats(ms):
+    return {"mean": sum(ms) / len(ms), "median": statistics.median(ms), "min": min(ms)}
+
+
+def summarize(w, w_name, step_ms, kernel_ms, peaks):
+    """Whole-step rate and the dominant kernel's roofline for one timed run."""
+    flops, kv_bytes = work_units(w)
+    is_decode = w_name == "bf16_decode"
+    pre = [k[1] for k in kernel_ms]
+    dec = [k[2] for k in kernel_ms if k[2] >= 0]
+    ms = sum(step_ms) / len(step_ms)
+    if is_decode:
+        dom = sum(dec) / len(dec)
+        achieved = kv_bytes / (dom * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "kernel": "pva_decode_kernel",
+                "peak_source": peaks["source"] + " hbm_gbs"}
+        value, unit = kv_bytes / (ms * 1e-3) / 1e9, "GB/s"
+    else:
+        dom = sum(pre) / len(pre)
+        achieved = flops / (dom * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "kernel": dominant_kernel(w),
+                "peak_source": peaks["source"] + " bf16_tflops (burst: kernel timed alone)"}
+        value, unit = flops / (ms * 1e-3) / 1e12, "TFLOP/s"
+    kms = {"scheduler": sum(k[0] for k in kernel_ms) / len(kernel_ms),
+           "prefill": sum(pre) / len(pre), "decode": (sum(dec) / len(dec)) if dec else None}
+    kmed = {"prefill": statistics.median(pre), "decode": statistics.median(dec) if dec else None}
+    return {"value": value, "unit": unit, "ms_per_step": ms, "step_ms": step_stats(step_ms),
+            "kernel_ms": kms, "kernel_ms_median": kmed, "roofline": roof,
+            "flops_per_step": flops, "kv_bytes_per_step": kv_bytes}
+
+
+def make_forward(pva, w, out):
+    H, Hkv, d, dv = w["num_heads"], w["kv_num_heads"], w["head_size"], w["v_head_size"]
+
+    def forward(q, k, v, cq, ck, o, s):
+        if w["window"] > 0:
+            pva.pva_forward_local(q, k, v, cq, ck, o, w["B"], H, Hkv, d, dv, w["scale"],
+                                  int(w["is_causal"]), w["softcap"], w["window"], stream=s)
+        else:
+            pva.pva_forward(q, k, v, cq, ck, o, w["B"], H, Hkv, d, dv, w["scale"],
+                            int(w["is_causal"]), w["softcap"], stream=s)
+
+    def step(s):
+        forward(w["q"], w["k"], w["v"], w["cu_q"], w["cu_kv"], out, s)
+    return forward, step
+
+
+def bench_other_config(pva, w_name, dev, steps, warmup, flush, peaks, local):
+    """One more workload in the same process (device-timed steps only), for
+    the record beside the headline line."""
+    import torch
+
+    from gqa_attention_cu_gb300 import workloads
+    w = workloads.make(w_name, seed=0, device=str(dev))
+    out = torch.empty(w["q"].shape[0], w["num_heads"], w["v_head_size"], dtype=w["q"].dtype,
+                      device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    _, step = make_forward(pva, w, out)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step(stream)
+    torch.cuda.synchronize(dev)
+    if pva.pva_get_status(stream) != 0:
+        raise SystemExit(f"device status bits set during {w_name} warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    step_ms, kernel_ms = time_steps(pva, step, stream, dev, steps, flush)
+    clk = clocks.stop()
+    if pva.pva_get_status(stream) != 0:
+        raise SystemExit(f"device status bits set during {w_name}")
+    rec = summarize(w, w_name, step_ms, kernel_ms, peaks)
+    rec["workload"] = WORKLOAD_TEXT[w_name]
+    rec["clocks"] = clk
+    rec["gpu_launches"] = launches_per_step(w) * steps
+    del w, out
+    torch.cuda.empty_cache()
+    return rec
+
+
+OTHER_CONFIGS = ("bf16_chunked", "bf16_decode", "bf16_longctx")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -490,6 +676,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-seconds", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the other configs measured beside the default line")
     ap.add_argument("--batch", type=int, default=None,
                     help="draw only this many sequences of the workload's recipe "
                          "(smaller cases for profiler captures; not a bench line)")
@@ -519,23 +707,13 @@ def main():
         bench_kvcache(args, rank, world, local, dev)
         return
     w = workloads.make(w_name, seed=rank, device=str(dev), B=args.batch)
-    H, Hkv, d, dv = w["num_heads"], w["kv_num_heads"], w["head_size"], w["v_head_size"]
+    H, dv = w["num_heads"], w["v_head_size"]
     flops, kv_bytes = work_units(w)
     is_decode = w_name == "bf16_decode"
     stream = torch.cuda.Stream(device=dev)
     out = torch.empty(w["q"].shape[0], H, dv, dtype=w["q"].dtype, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
-    def forward(q, k, v, cq, ck, o, s):
-        if w["window"] > 0:
-            pva.pva_forward_local(q, k, v, cq, ck, o, w["B"], H, Hkv, d, dv, w["scale"],
-                                  int(w["is_causal"]), w["softcap"], w["window"], stream=s)
-        else:
-            pva.pva_forward(q, k, v, cq, ck, o, w["B"], H, Hkv, d, dv, w["scale"],
-                            int(w["is_causal"]), w["softcap"], stream=s)
-
-    def step(s):
-        forward(w["q"], w["k"], w["v"], w["cu_q"], w["cu_kv"], out, s)
+    forward, step = make_forward(pva, w, out)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -544,37 +722,30 @@ def main():
     if pva.pva_get_status(stream) != 0:
         raise SystemExit("device status bits set during warm-up")
 
-    launches_per_step = 3 if w["dtype"] != "f32" and (H // Hkv) in (1, 2, 4, 8) else 2
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    kernel_ms = []
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.5)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    pva.pva_profile(True)
     wall0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            flush.fill_(i & 0xff)  # L2 flush: 256 MB write between steps
-            starts[i].record(stream)
-            step(stream)
-            ends[i].record(stream)
-            kernel_ms.append(pva.pva_kernel_times())
-    torch.cuda.synchronize(dev)
+    step_ms, kernel_ms = time_steps(pva, step, stream, dev, args.steps, flush)
     wall = time.perf_counter() - wall0
-    pva.pva_profile(False)
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
     job_flops = sum_over_ranks(flops, world, dev)
     job_kv = sum_over_ranks(kv_bytes, world, dev)
     if pva.pva_get_status(stream) != 0:
         raise SystemExit("device status bits set during the timed steps")
+    peaks = measured_peaks()
+    rec = summarize(w, w_name, step_ms, kernel_ms, peaks)
+
+    # The same steps without the L2 flush (inputs partly L2-resident from the
+    # previous step): reported beside the cold-L2 figures, never as `value`.
+    warm_ms, warm_kernel_ms = time_steps(pva, step, stream, dev, args.steps, None)
+    warm = summarize(w, w_name, warm_ms, warm_kernel_ms, peaks)
 
     # ---- end to end through the public API with host buffers ---------------
     host = {k: w[k].cpu().pin_memory() for k in ("q", "k", "v", "cu_q", "cu_kv")}
@@ -599,34 +770,17 @@ def main():
                 e2e_ms.append(a.elapsed_time(b))
     e2e = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world, dev)
 
-    peaks = measured_peaks()
-    pre_ms = [k[1] for k in kernel_ms]
-    dec_ms = [k[2] for k in kernel_ms if k[2] >= 0]
+    unit = rec["unit"]
     if is_decode:
-        unit = "GB/s"
         value = job_kv / (ms * 1e-3) / 1e9
         e2e_v = job_kv / (e2e * 1e-3) / 1e9
-        dom_ms = sum(dec_ms) / len(dec_ms)
-        achieved = kv_bytes / (dom_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"],
-                "traffic": recorded_traffic("decode_bf16_d128_g4"),
-                "kernel": "pva_decode_kernel", "peak_source": peaks["source"] + " hbm_gbs"}
+        traffic_key = "decode_bf16_d128_g4"
     else:
-        unit = "TFLOP/s"
         value = job_flops / (ms * 1e-3) / 1e12
         e2e_v = job_flops / (e2e * 1e-3) / 1e12
-        dom_ms = sum(pre_ms) / len(pre_ms)
-        achieved = flops / (dom_ms * 1e-3) / 1e12
-        key = "bf16_tflops"
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks[key], "unit": "TFLOP/s",
-                "frac": achieved / peaks[key],
-                "traffic": recorded_traffic(f"prefill_{w_name}"),
-                "kernel": ("pva_prefill_f32_kernel" if w["dtype"] == "f32" else
-                           "pva_prefill_pair_kernel"
-                           if w["head_size"] == w["v_head_size"] and w["head_size"] in (64, 128)
-                           else "pva_prefill_tc_kernel"),
-                "peak_source": peaks["source"] + " " + key + " (burst: kernel timed alone)"}
+        traffic_key = f"prefill_{w_name}"
+    roof = dict(rec["roofline"])
+    roof["traffic"] = recorded_traffic(traffic_key)
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -637,19 +791,34 @@ def main():
                    if not is_decode else "flushed between steps; K/V (4.6 GB) exceed L2",
                    "tokens_q": int(w["cu_q"][-1]), "tokens_kv": int(w["cu_kv"][-1]),
                    "flops_per_step": flops, "kv_bytes_per_step": kv_bytes,
-                   "kernel_ms": {"scheduler": sum(k[0] for k in kernel_ms) / len(kernel_ms),
-                                 "prefill": sum(pre_ms) / len(pre_ms),
-                                 "decode": (sum(dec_ms) / len(dec_ms)) if dec_ms else None},
+                   "kernel_ms": rec["kernel_ms"], "kernel_ms_median": rec["kernel_ms_median"],
+                   "step_ms": rec["step_ms"],
                    "parallelism": f"replicas x{world} (independent batches per GPU)"},
         "roofline": roof,
+        "warm_l2": {"value": warm["value"], "unit": unit, "step_ms": warm["step_ms"],
+                    "kernel_ms": warm["kernel_ms"], "frac": warm["roofline"]["frac"],
+                    "note": "same steps without the L2 flush; not the headline"},
         "e2e": {"value": e2e_v, "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": clk,
         "wall_s_timed_region": wall,
     }
+    del host, dbuf, out_host
+    # The other configs, each in its own timed region, beside the headline.
+    if (rank == 0 and world == 1 and w_name == "bf16_prefill" and not args.batch
+            and not args.no_other_configs):
+        del w, out
+        torch.cuda.empty_cache()
+        others = {}
+        for name in OTHER_CONFIGS:
+            others[name] = bench_other_config(pva, name, dev, args.steps, args.warmup, flush,
+                                              peaks, local)
+        line["other_configs"] = others
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w_name)
+        if w_name == "bf16_prefill" and world == 1:
+            line["cpu_baseline"]["fp32_small"] = fp32_oracle_check(pva, dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
