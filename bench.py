@@ -448,32 +448,23 @@ def bench_kvcache(args, rank, world, local, dev):
     torch.cuda.synchronize(dev)
     if pva.pva_get_status(stream) != 0:
         raise SystemExit("device status bits set during warm-up")
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    kernel_ms = []
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.5)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    pva.pva_profile(True)
+
+    def fwd(s):
+        step(c["q"], c["k_new"], c["v_new"], c["seqlens_k"], s)
     wall0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            flush.fill_(i & 0xff)
-            starts[i].record(stream)
-            step(c["q"], c["k_new"], c["v_new"], c["seqlens_k"], stream)
-            ends[i].record(stream)
-            kernel_ms.append(pva.pva_kernel_times())
-    torch.cuda.synchronize(dev)
+    step_ms, _ = time_steps(pva, fwd, stream, dev, args.steps, flush)
     wall = time.perf_counter() - wall0
-    pva.pva_profile(False)
     if world > 1:
         torch.distributed.barrier()
+    _, kernel_ms = time_steps(pva, fwd, stream, dev, args.steps, flush, profile=True)
     clk = clocks.stop()
-    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps,
-                        world, dev)
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
     job_kv = sum_over_ranks(kv_bytes, world, dev)
     if pva.pva_get_status(stream) != 0:
         raise SystemExit("device status bits set during the timed steps")
@@ -558,16 +549,20 @@ def launches_per_step(w):
     return 3 if dec else 2
 
 
-def time_steps(pva, forward, stream, dev, steps, flush):
+def time_steps(pva, forward, stream, dev, steps, flush, profile=False):
     """`steps` device-timed calls (CUDA events on the launching stream); with
     `flush` a 256 MB buffer is written between calls (cold L2).  Returns the
-    per-step times and the per-kernel times of each call."""
+    per-step times and, with `profile`, the per-kernel times of each call
+    (the library then records events between its kernels, which keeps a
+    kernel from starting its set-up while the one before it finishes, so
+    step times of a profiled pass are not the step rate)."""
     import torch
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     kernel_ms = []
     torch.cuda.synchronize(dev)
-    pva.pva_profile(True)
+    if profile:
+        pva.pva_profile(True)
     with torch.cuda.stream(stream):
         for i in range(steps):
             if flush is not None:
@@ -575,9 +570,11 @@ def time_steps(pva, forward, stream, dev, steps, flush):
             starts[i].record(stream)
             forward(stream)
             ends[i].record(stream)
-            kernel_ms.append(pva.pva_kernel_times())
+            if profile:
+                kernel_ms.append(pva.pva_kernel_times())
     torch.cuda.synchronize(dev)
-    pva.pva_profile(False)
+    if profile:
+        pva.pva_profile(False)
     return [s.elapsed_time(e) for s, e in zip(starts, ends)], kernel_ms
 
 
@@ -651,7 +648,8 @@ def bench_other_config(pva, w_name, dev, steps, warmup, flush, peaks, local):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    step_ms, kernel_ms = time_steps(pva, step, stream, dev, steps, flush)
+    step_ms, _ = time_steps(pva, step, stream, dev, steps, flush)
+    _, kernel_ms = time_steps(pva, step, stream, dev, steps, flush, profile=True)
     clk = clocks.stop()
     if pva.pva_get_status(stream) != 0:
         raise SystemExit(f"device status bits set during {w_name}")
@@ -729,7 +727,7 @@ def main():
         dist.barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
-    step_ms, kernel_ms = time_steps(pva, step, stream, dev, args.steps, flush)
+    step_ms, _ = time_steps(pva, step, stream, dev, args.steps, flush)
     wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
@@ -739,12 +737,16 @@ def main():
     job_kv = sum_over_ranks(kv_bytes, world, dev)
     if pva.pva_get_status(stream) != 0:
         raise SystemExit("device status bits set during the timed steps")
+    # Per-kernel times (the roofline's denominator) from a separate pass of
+    # the same steps with the library's kernel events on.
+    _, kernel_ms = time_steps(pva, step, stream, dev, args.steps, flush, profile=True)
     peaks = measured_peaks()
     rec = summarize(w, w_name, step_ms, kernel_ms, peaks)
 
     # The same steps without the L2 flush (inputs partly L2-resident from the
     # previous step): reported beside the cold-L2 figures, never as `value`.
-    warm_ms, warm_kernel_ms = time_steps(pva, step, stream, dev, args.steps, None)
+    warm_ms, _ = time_steps(pva, step, stream, dev, args.steps, None)
+    _, warm_kernel_ms = time_steps(pva, step, stream, dev, args.steps, None, profile=True)
     warm = summarize(w, w_name, warm_ms, warm_kernel_ms, peaks)
 
     # ---- end to end through the public API with host buffers ---------------

@@ -423,15 +423,18 @@ int forward_impl(const Spec& s, void* stream_) {
     prof_mark(2, stream);
     return PVA_OK;
   }
-  e = tc_paired(s.d, s.dv) ? launch_prefill_pair(p, s.dtype, tq, tk, tv, to, num_sms, stream)
-                           : launch_prefill_tc(p, s.dtype, tq, tk, tv, num_sms, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
-  prof_mark(2, stream);
+  // The decode kernel goes first: a batch without single-row sequences gives
+  // it no units, and it then exits while the scheduler's successor chain is
+  // still starting, instead of adding a launch after the prefill kernel.
   if (plan.decode) {
     e = launch_decode(p, s.dtype, dk, dvm, num_sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "split-KV decode launch");
-    prof_mark(3, stream);
+    prof_mark(2, stream);
   }
+  e = tc_paired(s.d, s.dv) ? launch_prefill_pair(p, s.dtype, tq, tk, tv, to, num_sms, stream)
+                           : launch_prefill_tc(p, s.dtype, tq, tk, tv, num_sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
+  prof_mark(plan.decode ? 3 : 2, stream);
   return PVA_OK;
 }
 
@@ -622,8 +625,13 @@ int pva_kernel_times(float* ms, int capacity) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   ms[0] = ms[1] = ms[2] = -1.0f;
   cudaEventElapsedTime(&ms[0], g_prof.ev[0], g_prof.ev[1]);
-  cudaEventElapsedTime(&ms[1], g_prof.ev[1], g_prof.ev[2]);
-  if (g_prof.decode) cudaEventElapsedTime(&ms[2], g_prof.ev[2], g_prof.ev[3]);
+  if (g_prof.decode) {
+    // launch order: scheduler, decode, prefill
+    cudaEventElapsedTime(&ms[2], g_prof.ev[1], g_prof.ev[2]);
+    cudaEventElapsedTime(&ms[1], g_prof.ev[2], g_prof.ev[3]);
+  } else {
+    cudaEventElapsedTime(&ms[1], g_prof.ev[1], g_prof.ev[2]);
+  }
   return PVA_OK;
 }
 

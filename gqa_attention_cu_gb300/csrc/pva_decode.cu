@@ -187,7 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   __syncthreads();
-  wait_prior_grid();  // scheduler lists and the prefill kernel's writes are complete
+  wait_prior_grid();  // the scheduler's work lists are complete from here on
+  allow_next_grid();  // the prefill kernel may start its set-up
   const SchedHeader h = *reinterpret_cast<const SchedHeader*>(p.ws + kWsHeader);
 
   if (warp == 0) {

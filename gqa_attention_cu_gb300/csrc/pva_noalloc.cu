@@ -179,13 +179,13 @@ extern "C" int pva_forward_noalloc(const void* q, const void* k, const void* v,
     e = launch_prefill_f32(p, ds.num_sms, stream);
     return e == cudaSuccess ? PVA_OK : cuda_fail(e, "fp32 attention launch");
   }
+  if (plan.decode) {  // decode first, as pva_forward orders them
+    e = launch_decode(p, dtype, dk, dvm, ds.num_sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "split-KV decode launch");
+  }
   e = tc_paired(head_size, v_head_size)
           ? launch_prefill_pair(p, dtype, tq, tk, tv, to, ds.num_sms, stream)
           : launch_prefill_tc(p, dtype, tq, tk, tv, ds.num_sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
-  if (plan.decode) {
-    e = launch_decode(p, dtype, dk, dvm, ds.num_sms, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "split-KV decode launch");
-  }
   return PVA_OK;
 }
