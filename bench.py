@@ -44,6 +44,10 @@ WORKLOAD_TEXT = {
     "fp32_small": "fp32 non-causal: L={17,64,1,130}, H=Hkv=4, d=dv=64, scale 1/8",
     "bf16_mla": "bf16 causal prefill, q.k wider than v: B=8, L_q=L_kv~U[512,4096], H=Hkv=32, "
                 "d=192, dv=128, N(0,1)",
+    "bf16_decode_g16": "bf16 decode, 16 query heads per kv head: B=256, L_q=1, "
+                       "L_kv~U[512,8192], H=32, Hkv=2, d=128, causal",
+    "bf16_decode_mla": "bf16 decode, q.k wider than v: B=256, L_q=1, L_kv~U[512,8192], H=32, "
+                       "Hkv=8, d=192, dv=128, causal",
     "bf16_window": "bf16 causal GQA prefill with a local window of 4096 keys: B=4, "
                    "L~logU[8192,32768], H=32, Hkv=8, d=dv=128, N(0,1)",
     "bf16_kvcache_decode": "bf16 GroupQueryAttention decode step on a BNSH KV cache of capacity "
@@ -259,7 +263,7 @@ class OracleSampler:
 
     def value(self, secs: float, pairs: int):
         sp = self.spec
-        if self.name == "bf16_decode":
+        if self.name.startswith("bf16_decode"):
             # every visible pair of a kv head's G query rows reads one K and V row;
             # count each K/V row once per kv head, as the GPU arm does
             kv = pairs / (sp.num_heads // sp.kv_num_heads) * (sp.head_size + sp.v_head_size) * 2
@@ -544,8 +548,7 @@ def launches_per_step(w):
     """Kernels one pva_forward launches: scheduler, prefill, and the split-KV
     decode kernel for the shapes it serves."""
     G = w["num_heads"] // w["kv_num_heads"]
-    dec = (w["dtype"] != "f32" and G in (1, 2, 4, 8) and w["head_size"] == w["v_head_size"]
-           and w["head_size"] in (64, 128, 256))
+    dec = w["dtype"] != "f32" and G in (1, 2, 4, 8, 16)
     return 3 if dec else 2
 
 
@@ -585,7 +588,7 @@ def step_stats(ms):
 def summarize(w, w_name, step_ms, kernel_ms, peaks):
     """Whole-step rate and the dominant kernel's roofline for one timed run."""
     flops, kv_bytes = work_units(w)
-    is_decode = w_name == "bf16_decode"
+    is_decode = w_name.startswith("bf16_decode")
     pre = [k[1] for k in kernel_ms]
     dec = [k[2] for k in kernel_ms if k[2] >= 0]
     ms = sum(step_ms) / len(step_ms)
@@ -707,7 +710,7 @@ def main():
     w = workloads.make(w_name, seed=rank, device=str(dev), B=args.batch)
     H, dv = w["num_heads"], w["v_head_size"]
     flops, kv_bytes = work_units(w)
-    is_decode = w_name == "bf16_decode"
+    is_decode = w_name.startswith("bf16_decode")
     stream = torch.cuda.Stream(device=dev)
     out = torch.empty(w["q"].shape[0], H, dv, dtype=w["q"].dtype, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -776,7 +779,7 @@ def main():
     if is_decode:
         value = job_kv / (ms * 1e-3) / 1e9
         e2e_v = job_kv / (e2e * 1e-3) / 1e9
-        traffic_key = "decode_bf16_d128_g4"
+        traffic_key = "decode_bf16_d128_g4" if w_name == "bf16_decode" else f"decode_{w_name}"
     else:
         value = job_flops / (ms * 1e-3) / 1e12
         e2e_v = job_flops / (e2e * 1e-3) / 1e12

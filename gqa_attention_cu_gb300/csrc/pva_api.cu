@@ -182,9 +182,10 @@ int check_and_plan(const void* q, const void* k, const void* v, const int32_t* c
     const uintptr_t mis = (uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)out;
     if (mis & 15) return fail(PVA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
     plan->tensor_core = true;
-    // The split-KV decode kernel covers d == dv in {64, 128, 256}; other
-    // shapes take their single-row sequences through the prefill kernel.
-    plan->decode = (G == 1 || G == 2 || G == 4 || G == 8) && d == dv && (d == 64 || d == 128 || d == 256);
+    // The split-KV decode kernel covers every head-size pair of the
+    // tensor-core path with G in {1, 2, 4, 8, 16}; other groupings take their
+    // single-row sequences through the prefill kernel.
+    plan->decode = G == 1 || G == 2 || G == 4 || G == 8 || G == 16;
     plan->sched = SchedConfig{(kTcRows / G) * tc_tiles_per_item(d, dv), Hkv, tc_block_n(d, dv),
                               plan->decode ? 1 : 0, 0};
   }
@@ -377,7 +378,7 @@ int forward_impl(const Spec& s, void* stream_) {
               PVA_OK)
         return rc;
       if (plan.decode) {
-        const int tkeys = decode_tile_keys(s.d);
+        const int tkeys = decode_tile_keys(s.d, s.dv);
         if ((rc = encode_plane_map(&dk, k, s.dtype, s.d, cs.cap, planes, s.d, tkeys,
                                    false)) != PVA_OK ||
             (rc = encode_plane_map(&dvm, v, s.dtype, s.dv, cs.cap, planes, s.dv, tkeys,
@@ -389,7 +390,7 @@ int forward_impl(const Spec& s, void* stream_) {
           (rc = encode_map(&tv, v, s.dtype, s.dv, s.Hkv, 64, 1, bn, true)) != PVA_OK)
         return rc;
       if (plan.decode) {
-        const int tkeys = decode_tile_keys(s.d);
+        const int tkeys = decode_tile_keys(s.d, s.dv);
         if ((rc = encode_map(&dk, k, s.dtype, s.d, s.Hkv, s.d, 1, tkeys, false)) != PVA_OK ||
             (rc = encode_map(&dvm, v, s.dtype, s.dv, s.Hkv, s.dv, 1, tkeys, false)) != PVA_OK)
           return rc;

@@ -1,5 +1,6 @@
 // Split-KV decode for sequences with a single query token (L_q == 1), bf16 or
-// f16, head size d = dv in {64, 128, 256}, H/Hkv = G in {1, 2, 4, 8}.
+// f16, head sizes (d, dv) in {(64,64), (96,96), (128,128), (192,192),
+// (256,256), (192,128)}, H/Hkv = G in {1, 2, 4, 8, 16}.
 //
 // With one query row the tail-aligned causal frontier (packed_varlen_
 // attention.rs, "Causal alignment") is L_kv - 1, so every key is visible and
@@ -14,12 +15,15 @@
 //               publishes each decoded unit through a shared-memory ring, and
 //               streams its K and V tiles of TK keys (16 KB each, rows of d
 //               contiguous elements) into a 4-stage ring.
-//   warps 1..8  compute.  A round covers R = 32/G keys x G heads = 32
-//               (key, head) pairs: lane l owns d/32 consecutive dims of every
-//               key, forms the 32 partial dot products, and a reduce-scatter
-//               butterfly (warp shuffles) leaves the full score of pair l in
-//               lane l.  Online softmax per head, probabilities shared
-//               through shared memory, O accumulated per lane over its dims.
+//   warps 1..8  compute.  A warp serves GW = min(G, 8) heads; with G = 16
+//               warps 1..4 take heads 0..7 and warps 5..8 heads 8..15 of the
+//               same tiles.  A round covers R = 32/GW keys x GW heads = 32
+//               (key, head) pairs: lane l owns DPL consecutive dims of every
+//               key (DPL = 2, 4 or 8; lanes past the head size hold zeros), forms
+//               the 32 partial dot products, and a reduce-scatter butterfly
+//               (warp shuffles) leaves the full score of pair l in lane l.
+//               Online softmax per head, probabilities shared through shared
+//               memory, O accumulated per lane over its dims of V.
 //   end of unit the 8 warps' (max, sum, O) are merged in a fixed order;
 //               an unsplit unit writes the output row; a split unit writes
 //               its fp32 partial and the last split to finish (device-wide
@@ -38,22 +42,35 @@ constexpr int kStages = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kUnitSlots = 4;
 
-template <int D, int G>
+// Dims per lane for a head size (the smallest of 2, 4, 8 that covers it
+// with 32 lanes); lanes [D / DPL, 32) hold no dims.
+__host__ __device__ constexpr int dims_per_lane(int D) { return D <= 64 ? 2 : D <= 128 ? 4 : 8; }
+
+template <int DK, int DV, int G>
 struct DecCfg {
-  static constexpr int TK = decode_tile_keys(D);   // keys per tile
-  static constexpr int DPL = D / 32;               // dims per lane
-  static constexpr int R = 32 / G;                 // keys per round
+  static constexpr int GW = G < 8 ? G : 8;         // heads per warp
+  static constexpr int HG = G / GW;                // head groups
+  static constexpr int NWG = kComputeWarps / HG;   // warps per head group
+  static constexpr int TK = decode_tile_keys(DK, DV);  // keys per tile
+  static constexpr int DPLK = dims_per_lane(DK), DPLV = dims_per_lane(DV);
+  static constexpr int LK = DK / DPLK, LV = DV / DPLV;  // lanes holding dims
+  static constexpr int R = 32 / GW;                // keys per round
   static constexpr int RPT = TK / R;               // rounds per tile
-  static constexpr int TILE_BYTES = TK * D * 2;
+  static constexpr int K_BYTES = TK * DK * 2;
+  static constexpr int V_BYTES = TK * DV * 2;
+  static constexpr int STAGE = K_BYTES + V_BYTES;
   static constexpr int OFF_KV = 0;
-  static constexpr int OFF_O = kStages * 2 * TILE_BYTES;             // [8][G][D] fp32
-  static constexpr int OFF_ML = OFF_O + kComputeWarps * G * D * 4;   // [8][G] m, [8][G] l
-  static constexpr int OFF_P = OFF_ML + 2 * kComputeWarps * G * 4;   // [8][32] p
-  static constexpr int OFF_A = OFF_P + kComputeWarps * 32 * 4;       // [8][G] alpha
-  static constexpr int OFF_BAR = OFF_A + kComputeWarps * G * 4;
+  static constexpr int OFF_O = kStages * STAGE;                       // [8][GW][DV] fp32
+  static constexpr int OFF_ML = OFF_O + kComputeWarps * GW * DV * 4;  // [8][GW] m, [8][GW] l
+  static constexpr int OFF_P = OFF_ML + 2 * kComputeWarps * GW * 4;   // [8][32] p
+  static constexpr int OFF_A = OFF_P + kComputeWarps * 32 * 4;        // [8][GW] alpha
+  static constexpr int OFF_BAR = OFF_A + kComputeWarps * GW * 4;
   static constexpr int OFF_UNITS = OFF_BAR + 2 * kStages * 8 + 2 * kUnitSlots * 8;
   static constexpr int SMEM = OFF_UNITS + kUnitSlots * 64 + 128;
-  static_assert(RPT >= 1, "tile shorter than a round");
+  static_assert(G % GW == 0 && kComputeWarps % HG == 0, "head groups");
+  static_assert(DK % DPLK == 0 && DV % DPLV == 0, "dims per lane");
+  static_assert(RPT >= 1 && TK % R == 0, "tile shorter than a round");
+  static_assert(K_BYTES % 128 == 0 && V_BYTES % 128 == 0, "tile alignment");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -148,18 +165,18 @@ __device__ __forceinline__ void load_probs(const float* src, float (&p)[G]) {
   }
 }
 
-template <typename T, int D, int G>
+template <typename T, int DK, int DV, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     pva_decode_kernel(AttnParams p, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v) {
-  using C = DecCfg<D, G>;
-  constexpr int TK = C::TK, DPL = C::DPL, R = C::R;
+  using C = DecCfg<DK, DV, G>;
+  constexpr int TK = C::TK, DPLK = C::DPLK, DPLV = C::DPLV, R = C::R, GW = C::GW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                              ~uintptr_t(127));
   float* sO = reinterpret_cast<float*>(smem + C::OFF_O);
   float* sM = reinterpret_cast<float*>(smem + C::OFF_ML);
-  float* sL = sM + kComputeWarps * G;
+  float* sL = sM + kComputeWarps * GW;
   float* sP = reinterpret_cast<float*>(smem + C::OFF_P);
   float* sA = reinterpret_cast<float*>(smem + C::OFF_A);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -228,11 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = cnt % kStages;
           if (!(ok = mbar_wait(&empty[st], ((cnt / kStages) & 1) ^ 1, abort, status))) break;
           const int k0 = tile_row<TK>(p, un, j, total_kv);
-          uint8_t* dk = smem + C::OFF_KV + st * 2 * C::TILE_BYTES;
-          mbar_arrive_expect_tx(&full[st], 2 * C::TILE_BYTES);
+          uint8_t* dk = smem + C::OFF_KV + st * C::STAGE;
+          mbar_arrive_expect_tx(&full[st], C::STAGE);
           const int2 yz = kv_tma_yz(p, un.b, un.g, un.kv_start, k0);
           tma_load_3d(dk, &tmap_k, &full[st], 0, yz.x, yz.y);
-          tma_load_3d(dk + C::TILE_BYTES, &tmap_v, &full[st], 0, yz.x, yz.y);
+          tma_load_3d(dk + C::K_BYTES, &tmap_v, &full[st], 0, yz.x, yz.y);
           if (!decoded) {
             nx = decode_unit(p, h, u_next);
             decoded = true;
@@ -256,11 +273,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ compute
     const int cw = warp - 1;  // compute warp 0..7
+    const int hgrp = cw / C::NWG, cwg = cw % C::NWG;  // head group, warp within it
+    const int hbase = hgrp * GW;                       // first head of the group
     const float NEG_INF = __int_as_float(0xff800000);
     const bool capped = p.softcap != 0.0f;
     const float qmul = capped ? p.scale / p.softcap : p.scale * kLog2e;
     const float cap_mul = p.softcap * kLog2e;
-    const int my_r = lane / G;  // key of the (key, head) pair this lane owns after the reduce-scatter
+    const int my_r = lane / GW;  // key of the (key, head) pair this lane owns after the reduce-scatter
     T* out = static_cast<T*>(p.out);
     uint32_t cnt = 0;
     bool ok = true;
@@ -279,49 +298,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = un.u;
       const int nt = (un.ke - un.ks + TK - 1) / TK;
 
-      float q[G][DPL];
+      float q[GW][DPLK];
       {
         const T* Q = static_cast<const T*>(p.q);
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          const uint8_t* row = reinterpret_cast<const uint8_t*>(
-              Q + ((size_t)un.q_tok * p.H + (size_t)un.g * G + hh) * D);
-          load_dims<T, DPL>(row, lane, q[hh]);
+        for (int hh = 0; hh < GW; ++hh) {
+          if (lane < C::LK) {
+            const uint8_t* row = reinterpret_cast<const uint8_t*>(
+                Q + ((size_t)un.q_tok * p.H + (size_t)un.g * G + hbase + hh) * DK);
+            load_dims<T, DPLK>(row, lane, q[hh]);
+          } else {
 #pragma unroll
-          for (int e = 0; e < DPL; ++e) q[hh][e] *= qmul;
+            for (int e = 0; e < DPLK; ++e) q[hh][e] = 0.0f;
+          }
+#pragma unroll
+          for (int e = 0; e < DPLK; ++e) q[hh][e] *= qmul;
         }
       }
-      float acc[G][DPL];
+      float acc[GW][DPLV];
 #pragma unroll
-      for (int hh = 0; hh < G; ++hh)
+      for (int hh = 0; hh < GW; ++hh)
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[hh][e] = 0.0f;
+        for (int e = 0; e < DPLV; ++e) acc[hh][e] = 0.0f;
       float m_run = NEG_INF, l_part = 0.0f;
 
       for (int j = 0; j < nt; ++j, ++cnt) {
         const int st = cnt % kStages;
         ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (cnt / kStages) & 1, abort, status));
         if (!ok) break;
-        const uint8_t* sK = smem + C::OFF_KV + st * 2 * C::TILE_BYTES;
-        const uint8_t* sV = sK + C::TILE_BYTES;
+        const uint8_t* sK = smem + C::OFF_KV + st * C::STAGE;
+        const uint8_t* sV = sK + C::K_BYTES;
         const int k0 = tile_row<TK>(p, un, j, total_kv);
         const int base = k0 - un.kv_start;            // local key of tile row 0
         const int lo = un.ks + j * TK - base;          // visible tile rows [lo, hi)
         const int hi = min(un.ks + (j + 1) * TK, un.ke) - base;
-        for (int rd = cw; rd < C::RPT; rd += kComputeWarps) {
+        for (int rd = cwg; rd < C::RPT; rd += C::NWG) {
           const int r0 = rd * R;  // first tile row of this round
           float v[32];
 #pragma unroll
           for (int r = 0; r < R; ++r) {
-            float kf[DPL];
-            load_dims<T, DPL>(sK + (size_t)(r0 + r) * D * 2, lane, kf);
+            float kf[DPLK];
+            if (C::LK == 32 || lane < C::LK) {
+              load_dims<T, DPLK>(sK + (size_t)(r0 + r) * DK * 2, lane, kf);
+            } else {
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
+              for (int e = 0; e < DPLK; ++e) kf[e] = 0.0f;
+            }
+#pragma unroll
+            for (int hh = 0; hh < GW; ++hh) {
               float2 a = make_float2(0.0f, 0.0f);
 #pragma unroll
-              for (int e = 0; e < DPL; e += 2)
+              for (int e = 0; e < DPLK; e += 2)
                 a = ffma2(make_float2(q[hh][e], q[hh][e + 1]), make_float2(kf[e], kf[e + 1]), a);
-              v[r * G + hh] = a.x + a.y;
+              v[r * GW + hh] = a.x + a.y;
             }
           }
           // reduce-scatter: after the 5 steps lane l holds the full dot of pair l
@@ -340,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           x = (row >= lo && row < hi) ? x : NEG_INF;
           float mr = x;
 #pragma unroll
-          for (int o = G; o < 32; o <<= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+          for (int o = GW; o < 32; o <<= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
           const float m_new = fmaxf(m_run, mr);
           float alpha = 1.0f, pr = 0.0f;
           if (m_new != NEG_INF) {
@@ -350,24 +379,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = m_new;
           l_part = l_part * alpha + pr;
           sP[cw * 32 + lane] = pr;
-          if (lane < G) sA[cw * G + lane] = alpha;
+          if (lane < GW) sA[cw * GW + lane] = alpha;
           __syncwarp();
 #pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            const float a = sA[cw * G + hh];
+          for (int hh = 0; hh < GW; ++hh) {
+            const float a = sA[cw * GW + hh];
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[hh][e] *= a;
+            for (int e = 0; e < DPLV; ++e) acc[hh][e] *= a;
           }
 #pragma unroll
           for (int r = 0; r < R; ++r) {
-            float vf[DPL];
-            load_dims<T, DPL>(sV + (size_t)(r0 + r) * D * 2, lane, vf);
-            float pw[G];
-            load_probs<G>(sP + cw * 32 + r * G, pw);
+            float vf[DPLV];
+            if (C::LV == 32 || lane < C::LV) {
+              load_dims<T, DPLV>(sV + (size_t)(r0 + r) * DV * 2, lane, vf);
+            } else {
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh)
+              for (int e = 0; e < DPLV; ++e) vf[e] = 0.0f;
+            }
+            float pw[GW];
+            load_probs<GW>(sP + cw * 32 + r * GW, pw);
 #pragma unroll
-              for (int e = 0; e < DPL; e += 2) {
+            for (int hh = 0; hh < GW; ++hh)
+#pragma unroll
+              for (int e = 0; e < DPLV; e += 2) {
                 const float2 a = ffma2(make_float2(pw[hh], pw[hh]), make_float2(vf[e], vf[e + 1]),
                                        make_float2(acc[hh][e], acc[hh][e + 1]));
                 acc[hh][e] = a.x;
@@ -380,17 +414,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&empty[st]);
       }
 
-      // per-head sum over this warp's lanes, then merge the 8 warps
+      // per-head sum over this warp's lanes, then merge the warps of each
+      // head group
 #pragma unroll
-      for (int o = G; o < 32; o <<= 1) l_part += __shfl_xor_sync(0xffffffffu, l_part, o);
-      if (lane < G) {
-        sM[cw * G + lane] = m_run;
-        sL[cw * G + lane] = l_part;
+      for (int o = GW; o < 32; o <<= 1) l_part += __shfl_xor_sync(0xffffffffu, l_part, o);
+      if (lane < GW) {
+        sM[cw * GW + lane] = m_run;
+        sL[cw * GW + lane] = l_part;
       }
+      if (C::LV == 32 || lane < C::LV) {
 #pragma unroll
-      for (int hh = 0; hh < G; ++hh)
+        for (int hh = 0; hh < GW; ++hh)
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) sO[(cw * G + hh) * D + lane * DPL + e] = acc[hh][e];
+          for (int e = 0; e < DPLV; ++e)
+            sO[(cw * GW + hh) * DV + lane * DPLV + e] = acc[hh][e];
+      }
       // Every compute warp reaches this barrier, whether it finished its tiles
       // or gave up on a wait; the give-up decision is then read by all of
       // them at once, so no warp is ever left alone at a named barrier.
@@ -399,29 +437,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const int t = threadIdx.x - 32;  // 0..255
       const bool split = un.S > 1;
-      float* part = p.partials + (size_t)u * (G * D + 2 * G);
-      for (int e = t; e < G * D; e += kComputeWarps * 32) {
-        const int hh = e / D;
+      float* part = p.partials + (size_t)u * (G * DV + 2 * G);
+      for (int e = t; e < G * DV; e += kComputeWarps * 32) {
+        const int hh = e / DV;  // head within the kv group
+        const int grp = hh / GW, lh = hh - grp * GW, de = e - hh * DV;
+        const int w0 = grp * C::NWG;  // the warps that served this head
         float M = NEG_INF;
 #pragma unroll
-        for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, sM[w * G + hh]);
+        for (int w = 0; w < C::NWG; ++w) M = fmaxf(M, sM[(w0 + w) * GW + lh]);
         float Lsum = 0.0f, O = 0.0f;
         if (M != NEG_INF) {
 #pragma unroll
-          for (int w = 0; w < kComputeWarps; ++w) {
-            const float sc = ex2_approx(sM[w * G + hh] - M);
-            Lsum += sL[w * G + hh] * sc;
-            O += sO[w * G * D + e] * sc;
+          for (int w = 0; w < C::NWG; ++w) {
+            const float sc = ex2_approx(sM[(w0 + w) * GW + lh] - M);
+            Lsum += sL[(w0 + w) * GW + lh] * sc;
+            O += sO[((w0 + w) * GW + lh) * DV + de] * sc;
           }
         }
         if (!split) {
           const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
-          out[((size_t)un.q_tok * p.H + (size_t)un.g * G) * D + e] = static_cast<T>(O * inv);
+          out[((size_t)un.q_tok * p.H + (size_t)un.g * G) * DV + e] = static_cast<T>(O * inv);
         } else {
           part[e] = O;
-          if (e - hh * D == 0) {
-            part[G * D + hh] = M;
-            part[G * D + G + hh] = Lsum;
+          if (de == 0) {
+            part[G * DV + hh] = M;
+            part[G * DV + G + hh] = Lsum;
           }
         }
       }
@@ -436,23 +476,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         compute_bar_sync();
         if (s_last) {
           __threadfence();
-          const float* first = p.partials + (size_t)(u - un.s) * (G * D + 2 * G);
-          const size_t stride = G * D + 2 * G;
-          for (int e = t; e < G * D; e += kComputeWarps * 32) {
-            const int hh = e / D;
+          const float* first = p.partials + (size_t)(u - un.s) * (G * DV + 2 * G);
+          const size_t stride = G * DV + 2 * G;
+          for (int e = t; e < G * DV; e += kComputeWarps * 32) {
+            const int hh = e / DV;
             float M = NEG_INF;
-            for (int s = 0; s < un.S; ++s) M = fmaxf(M, __ldcg(first + s * stride + G * D + hh));
+            for (int s = 0; s < un.S; ++s) M = fmaxf(M, __ldcg(first + s * stride + G * DV + hh));
             float Lsum = 0.0f, O = 0.0f;
             if (M != NEG_INF) {
               for (int s = 0; s < un.S; ++s) {
                 const float* ps = first + s * stride;
-                const float sc = ex2_approx(__ldcg(ps + G * D + hh) - M);
-                Lsum += __ldcg(ps + G * D + G + hh) * sc;
+                const float sc = ex2_approx(__ldcg(ps + G * DV + hh) - M);
+                Lsum += __ldcg(ps + G * DV + G + hh) * sc;
                 O += __ldcg(ps + e) * sc;
               }
             }
             const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
-            out[((size_t)un.q_tok * p.H + (size_t)un.g * G) * D + e] = static_cast<T>(O * inv);
+            out[((size_t)un.q_tok * p.H + (size_t)un.g * G) * DV + e] = static_cast<T>(O * inv);
           }
         }
       }
@@ -462,24 +502,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 }
 
-template <typename T, int D, int G>
+template <typename T, int DK, int DV, int G>
 cudaError_t launch_dec(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                        int num_sms, cudaStream_t s) {
-  constexpr int smem = DecCfg<D, G>::SMEM;
-  auto kern = pva_decode_kernel<T, D, G>;
+  constexpr int smem = DecCfg<DK, DV, G>::SMEM;
+  auto kern = pva_decode_kernel<T, DK, DV, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return launch_dependent(kern, dim3(num_sms), dim3(kThreads), smem, s, p, tk, tv);
 }
 
-template <typename T, int D>
+template <typename T, int DK, int DV>
 cudaError_t launch_dec_g(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                          int num_sms, cudaStream_t s) {
   switch (p.G) {
-    case 1: return launch_dec<T, D, 1>(p, tk, tv, num_sms, s);
-    case 2: return launch_dec<T, D, 2>(p, tk, tv, num_sms, s);
-    case 4: return launch_dec<T, D, 4>(p, tk, tv, num_sms, s);
-    case 8: return launch_dec<T, D, 8>(p, tk, tv, num_sms, s);
+    case 1: return launch_dec<T, DK, DV, 1>(p, tk, tv, num_sms, s);
+    case 2: return launch_dec<T, DK, DV, 2>(p, tk, tv, num_sms, s);
+    case 4: return launch_dec<T, DK, DV, 4>(p, tk, tv, num_sms, s);
+    case 8: return launch_dec<T, DK, DV, 8>(p, tk, tv, num_sms, s);
+    case 16: return launch_dec<T, DK, DV, 16>(p, tk, tv, num_sms, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -487,12 +528,18 @@ cudaError_t launch_dec_g(const AttnParams& p, const CUtensorMap& tk, const CUten
 template <typename T>
 cudaError_t launch_dec_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                          int num_sms, cudaStream_t s) {
-  switch (p.d) {
-    case 64: return launch_dec_g<T, 64>(p, tk, tv, num_sms, s);
-    case 128: return launch_dec_g<T, 128>(p, tk, tv, num_sms, s);
-    case 256: return launch_dec_g<T, 256>(p, tk, tv, num_sms, s);
-    default: return cudaErrorInvalidValue;
+  if (p.d == p.dv) {
+    switch (p.d) {
+      case 64: return launch_dec_g<T, 64, 64>(p, tk, tv, num_sms, s);
+      case 96: return launch_dec_g<T, 96, 96>(p, tk, tv, num_sms, s);
+      case 128: return launch_dec_g<T, 128, 128>(p, tk, tv, num_sms, s);
+      case 192: return launch_dec_g<T, 192, 192>(p, tk, tv, num_sms, s);
+      case 256: return launch_dec_g<T, 256, 256>(p, tk, tv, num_sms, s);
+      default: return cudaErrorInvalidValue;
+    }
   }
+  if (p.d == 192 && p.dv == 128) return launch_dec_g<T, 192, 128>(p, tk, tv, num_sms, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace

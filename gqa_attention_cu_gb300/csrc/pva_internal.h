@@ -22,7 +22,7 @@ constexpr int kTcRows = 128;        // MMA rows per query tile (G heads x tokens
 constexpr int kF32TileTokens = 16;  // query tokens per fp32 work item
 constexpr int kF32KeyTile = 32;     // keys per fp32 key/value tile
 constexpr int kDecodeMaxSplits = 16;
-constexpr int kDecodeMaxGroup = 8;  // largest H/Hkv served by the split-KV decode kernel
+constexpr int kDecodeMaxGroup = 16;  // largest H/Hkv served by the split-KV decode kernel
 constexpr int kSortMax = 2048;      // sequences sorted on device; more keep input order
 
 // Query tiles per prefill work item: two 128-row tiles share each K/V tile
@@ -36,8 +36,11 @@ __host__ __device__ constexpr int tc_block_n(int d, int dv) { return tc_paired(d
 // Tokens per TMA store box of the paired kernel's output: one warp's 32 rows
 // (32 / G tokens x G heads) when G divides 32, else the whole 128-row tile.
 __host__ __device__ constexpr int out_box_tokens(int G) { return 32 % G == 0 ? 32 / G : kTcRows / G; }
-// Keys per decode key/value tile for head size D (16 KB of K per tile).
-__host__ __device__ constexpr int decode_tile_keys(int D) { return 8192 / D; }
+// Keys per decode key/value tile for head sizes DK (K) and DV (V): a power
+// of two with at most 16 KB of the wider of the two per tile.
+__host__ __device__ constexpr int decode_tile_keys(int DK, int DV) {
+  return (DK > DV ? DK : DV) <= 64 ? 128 : (DK > DV ? DK : DV) <= 128 ? 64 : 32;
+}
 
 // ---- workspace layout (int32 words) ----------------------------------------
 // [0..8)         SchedHeader of the latest call

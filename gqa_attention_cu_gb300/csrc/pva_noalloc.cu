@@ -164,7 +164,7 @@ extern "C" int pva_forward_noalloc(const void* q, const void* k, const void* v,
                          true)) != PVA_OK)
       return rc;
     if (plan.decode) {
-      const int tkeys = decode_tile_keys(head_size);
+      const int tkeys = decode_tile_keys(head_size, v_head_size);
       if ((rc = encode_map(&dk, ka, dtype, head_size, kv_num_heads, head_size, 1, tkeys,
                            false)) != PVA_OK ||
           (rc = encode_map(&dvm, va, dtype, v_head_size, kv_num_heads, v_head_size, 1, tkeys,

@@ -25,6 +25,9 @@ tests use):
                      N(0, 2).
 * ``bf16_mla``     : B = 8, L_q = L_kv ~ U{512..4096}, H = Hkv = 32,
                      d = 192, dv = 128 (q.k wider than v), causal, N(0, 1).
+* ``bf16_decode_g16``: the decode batch with H = 32, Hkv = 2 (16 query heads
+                     per kv head).
+* ``bf16_decode_mla``: the decode batch with d = 192, dv = 128, H = 32, Hkv = 8.
 * ``bf16_window``  : B = 4, L_q = L_kv = round(exp(U(ln 8192, ln 32768))),
                      H = 32, Hkv = 8, d = dv = 128, causal, local window 4096,
                      N(0, 1).
@@ -77,6 +80,12 @@ WORKLOADS = {
                              math.sqrt(2.0), "loguniform_self", params={"lo": 8192, "hi": 32768}),
     "bf16_mla": Workload("bf16_mla", 8, 32, 32, 192, 128, "bf16", True, 0.0, 0.0, 1.0,
                          "uniform_self", params={"lo": 512, "hi": 4096}),
+    # the decode batch with 16 query heads per kv head, and with MLA-style
+    # head sizes (q.k over 192 dims, v 128)
+    "bf16_decode_g16": Workload("bf16_decode_g16", 256, 32, 2, 128, 128, "bf16", True, 0.0, 0.0,
+                                1.0, "decode", params={"lo": 512, "hi": 8192}),
+    "bf16_decode_mla": Workload("bf16_decode_mla", 256, 32, 8, 192, 128, "bf16", True, 0.0, 0.0,
+                                1.0, "decode", params={"lo": 512, "hi": 8192}),
     "bf16_window": Workload("bf16_window", 4, 32, 8, 128, 128, "bf16", True, 0.0, 0.0, 1.0,
                             "loguniform_self", params={"lo": 8192, "hi": 32768}, window=4096),
     # one decode step against a fixed-capacity BNSH KV cache (pva_gqa_kvcache):

@@ -115,6 +115,36 @@ def test_prefill_extra_head_sizes(d, dv, G):
     check(out, oracle.attention(q, k, v, cq, ck, G * Hkv, Hkv, 0.0, True, 0.0), "bf16")
 
 
+# Split-KV decode for every head-size pair of the tensor-core path and every
+# grouping it serves (G = 16 runs as two head groups of 8), with keys enough
+# for several splits and the log-sum-exp combine.
+@pytest.mark.parametrize("d,dv", [(64, 64), (96, 96), (128, 128), (192, 192), (256, 256),
+                                  (192, 128)])
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+def test_split_kv_decode_every_shape_and_group(d, dv, G):
+    Hkv = 2 if G < 16 else 1
+    lq = [1, 1, 1, 1, 1, 1]
+    lkv = [1, 37, 700, 2500, 64, 6000]
+    q, k, v, cq, ck = workloads.make_packed(lq, lkv, G * Hkv, Hkv, d, dv, "bf16",
+                                            seed=3 * d + dv + G)
+    out = run_gpu(q, k, v, cq, ck, G * Hkv, Hkv, 0.0, True, 0.0)
+    check(out, oracle.attention(q, k, v, cq, ck, G * Hkv, Hkv, 0.0, True, 0.0), "bf16")
+
+
+@pytest.mark.parametrize("d,dv,G,dtype,softcap", [(96, 96, 16, "f16", 0.0),
+                                                 (192, 128, 4, "f16", 30.0),
+                                                 (128, 128, 16, "bf16", 5.0),
+                                                 (192, 192, 8, "bf16", 2.0)])
+def test_split_kv_decode_f16_and_softcap(d, dv, G, dtype, softcap):
+    # unit-variance inputs (the bf16 tolerance is set for them); a small
+    # softcap keeps the tanh far from linear
+    Hkv = 2
+    lq, lkv = [1, 1, 1, 40], [3000, 17, 900, 300]
+    q, k, v, cq, ck = workloads.make_packed(lq, lkv, G * Hkv, Hkv, d, dv, dtype, seed=d + G)
+    out = run_gpu(q, k, v, cq, ck, G * Hkv, Hkv, 0.0, True, softcap)
+    check(out, oracle.attention(q, k, v, cq, ck, G * Hkv, Hkv, 0.0, True, softcap), dtype)
+
+
 @pytest.mark.parametrize("d,dv,dtype,causal,softcap", [(96, 96, "f16", False, 0.0),
                                                       (192, 128, "bf16", True, 30.0),
                                                       (192, 128, "f16", False, 0.0)])
@@ -339,7 +369,7 @@ def sched_mirror(lq, lkv, H, Hkv, d, dtype, num_sms, dv=None):
         G = H // Hkv
         paired = d == dv and d in (64, 128)
         tile, units = (128 // G) * (2 if paired else 1), Hkv
-        dec = G in (1, 2, 4, 8) and d == dv and d in (64, 128, 256)
+        dec = G in (1, 2, 4, 8, 16)
     cap = min(B * Hkv * 16, 16384)
     INT_MAX = 2 ** 31 - 1
     chunk = INT_MAX
