@@ -169,7 +169,7 @@ int check_and_plan(const void* q, const void* k, const void* v, const int32_t* c
   if (dtype == PVA_F32) {
     if (d > 256 || dv > 256)
       return fail(PVA_ERR_UNSUPPORTED, "f32 path supports head sizes up to 256");
-    plan->sched = SchedConfig{kF32TileTokens, H, kF32KeyTile, 0, 0};
+    plan->sched = SchedConfig{kF32TileTokens, H, kF32KeyTile, 0, 0, 0};
   } else {
     const bool shape_ok = (d == dv && (d == 64 || d == 96 || d == 128 || d == 192 || d == 256)) ||
                           (d == 192 && dv == 128);
@@ -184,10 +184,16 @@ int check_and_plan(const void* q, const void* k, const void* v, const int32_t* c
     plan->tensor_core = true;
     // The split-KV decode kernel covers every head-size pair of the
     // tensor-core path with G in {1, 2, 4, 8, 16}; other groupings take their
-    // single-row sequences through the prefill kernel.
+    // single-row sequences through the prefill kernel.  For d == dv in
+    // {64, 128, 256} with G <= 8 it reads K/V at close to copy bandwidth and
+    // takes every single-row sequence; for the other shapes (G = 16, head
+    // sizes 96 and 192) it is limited by its arithmetic, and the scheduler
+    // gives it single-row sequences only when they are too few to keep every
+    // SM busy in the prefill kernel (which does not split keys).
     plan->decode = G == 1 || G == 2 || G == 4 || G == 8 || G == 16;
+    const bool tuned = G <= 8 && d == dv && (d == 64 || d == 128 || d == 256);
     plan->sched = SchedConfig{(kTcRows / G) * tc_tiles_per_item(d, dv), Hkv, tc_block_n(d, dv),
-                              plan->decode ? 1 : 0, 0};
+                              plan->decode ? 1 : 0, 0, plan->decode && !tuned ? 1 : 0};
   }
   const WsLayout L{B, Hkv};
   plan->int_bytes = L.int_words() * 4;

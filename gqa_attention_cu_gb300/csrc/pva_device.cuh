@@ -172,19 +172,39 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
+// try_wait without a suspend-time hint: the thread waits in hardware for a
+// short, implementation-defined time and is not parked.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase of `bar` with the given parity has completed.  Gives
 // up after PVA_WAIT_LIMIT_NS (or as soon as another role has given up, which
 // it signals through *abort): sets the abort flag and the device status bit
 // and returns false.  Every pipeline wait in this library goes through here.
-// Each attempt may sleep up to PVA_WAIT_SLICE_NS, so the limit is checked
-// with that granularity.
+// PARK: each attempt may park the thread for up to PVA_WAIT_SLICE_NS (so the
+// limit is checked with that granularity) -- the decode kernel's choice;
+// the tensor-core prefill kernels, whose hand-offs are latency-critical,
+// measured faster without it (1.5-4%).
+template <bool PARK = true>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status,
                                           uint64_t limit_ns = PVA_WAIT_LIMIT_NS) {
-  if (mbar_try_wait_sleep(bar, parity, PVA_WAIT_SLICE_NS)) return true;
+  auto attempt = [&]() {
+    return PARK ? mbar_try_wait_sleep(bar, parity, PVA_WAIT_SLICE_NS) : mbar_try_wait(bar, parity);
+  };
+  if (attempt()) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity, PVA_WAIT_SLICE_NS)) return true;
+    if (attempt()) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > limit_ns) {
       *abort = 1;

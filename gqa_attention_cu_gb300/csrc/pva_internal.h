@@ -112,6 +112,11 @@ struct SchedConfig {
   int block_n;         // keys per prefill key tile (cost model only)
   int decode_enabled;  // route L_q == 1 sequences to the decode kernel
   int num_sms;
+  // 1: route them there only when they are too few to fill the GPU through
+  // the prefill kernel -- (L_q == 1 sequences) x kv heads < 2 x SMs --
+  // because for this shape the tensor-core prefill kernel reads K/V faster
+  // once it has enough (sequence, kv head) items.
+  int decode_adaptive;
 };
 
 // ---- host helpers shared by the entry points (pva_api.cu) --------------------

@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       auto publish = [&](const ItemSlot& v) -> bool {
         const int sl = published % kItemSlots;
-        if (!mbar_wait(&bars->item_empty[sl], ((published / kItemSlots) & 1) ^ 1, abort, status))
+        if (!mbar_wait<false>(&bars->item_empty[sl], ((published / kItemSlots) & 1) ^ 1, abort, status))
           return false;
         bars->items[sl] = v;
         mbar_arrive(&bars->item_full[sl]);
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = publish(v))) break;
         if (v.n_tiles > 0) {
           const int g = v.unit;
-          if (!(ok = mbar_wait(&bars->q_empty, (items & 1) ^ 1, abort, status))) break;
+          if (!(ok = mbar_wait<false>(&bars->q_empty, (items & 1) ^ 1, abort, status))) break;
           mbar_arrive_expect_tx(&bars->q_full, q_bytes);
 #pragma unroll
           for (int t = 0; t < 2; ++t)
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kv = 0; kv < 2; ++kv, ++loads) {
               const int sl = loads % C::SLOTS;
-              if (!(ok = mbar_wait(&bars->ring_empty[sl], ((loads / C::SLOTS) & 1) ^ 1, abort,
+              if (!(ok = mbar_wait<false>(&bars->ring_empty[sl], ((loads / C::SLOTS) & 1) ^ 1, abort,
                                    status)))
                 break;
               uint8_t* dst = smem + C::OFF_RING + sl * C::KV_TILE;
@@ -241,10 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         publish(v);
       }
       // Drain: every copy this thread issued must land before the CTA exits.
-      if (items) mbar_wait(&bars->q_full, (items - 1) & 1, abort, status);
+      if (items) mbar_wait<false>(&bars->q_full, (items - 1) & 1, abort, status);
       for (int s = 0; s < C::SLOTS; ++s) {
         const uint32_t fills = loads > (uint32_t)s ? (loads - 1 - s) / C::SLOTS + 1 : 0;
-        if (fills) mbar_wait(&bars->ring_full[s], (fills - 1) & 1, abort, status);
+        if (fills) mbar_wait<false>(&bars->ring_full[s], (fills - 1) & 1, abort, status);
       }
     }
   } else if (warp == 1) {
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, status));
+      return __all_sync(0xffffffffu, mbar_wait<false>(bar, parity, abort, status));
     };
     auto wait_slot = [&](uint32_t L) -> bool {
       const bool r = wait(&bars->ring_full[L % C::SLOTS], (L / C::SLOTS) & 1);
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     while (ok) {
       const int isl = taken % kItemSlots;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->item_full[isl], (taken / kItemSlots) & 1,
+      ok = __all_sync(0xffffffffu, mbar_wait<false>(&bars->item_full[isl], (taken / kItemSlots) & 1,
                                              abort, status));
       if (!ok) break;
       const ItemSlot it = bars->items[isl];
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       for (int j = 0; j < n; ++j) {
         const uint32_t T_ = tiles + j;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[tq], T_ & 1, abort, status));
+        ok = __all_sync(0xffffffffu, mbar_wait<false>(&bars->s_full[tq], T_ & 1, abort, status));
         if (!ok) break;
         tc_fence_after();
         const int J = it.jb + j;            // key tile index within the sequence
@@ -497,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // epilogue: O / l -> out (rows of this item only)
       const uint32_t T_last = tiles + n - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[tq], T_last & 1, abort, status));
+      ok = __all_sync(0xffffffffu, mbar_wait<false>(&bars->o_ready[tq], T_last & 1, abort, status));
       if (!ok) break;
       tc_fence_after();
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive(&bars->stage_free[tq]);
             }
             ok = __all_sync(0xffffffffu,
-                            mbar_wait(&bars->stage_free[tq], stages & 1, abort, status));
+                            mbar_wait<false>(&bars->stage_free[tq], stages & 1, abort, status));
             if (!ok) break;
           }
           // Row r: 128 bytes in the 128-byte swizzled layout of the TMA box.
@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             mbar_arrive(&bars->stage_full[tq]);
             if (issuer) {
-              if (!(ok = mbar_wait(&bars->stage_full[tq], stages & 1, abort, status))) break;
+              if (!(ok = mbar_wait<false>(&bars->stage_full[tq], stages & 1, abort, status))) break;
               tma_store_3d(&tmap_o, stage, c - 32, it.unit * G, tok0);
               bulk_commit();
             }

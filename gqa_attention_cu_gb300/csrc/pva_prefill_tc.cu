@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       auto publish = [&](const ItemSlot& v) -> bool {
         const int sl = published % kItemSlots;
-        if (!mbar_wait(&bars->item_empty[sl], ((published / kItemSlots) & 1) ^ 1, abort, status))
+        if (!mbar_wait<false>(&bars->item_empty[sl], ((published / kItemSlots) & 1) ^ 1, abort, status))
           return false;
         bars->items[sl] = v;
         mbar_arrive(&bars->item_full[sl]);
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = publish(v))) break;
         if (v.n_tiles > 0) {
           const int g = v.unit;
-          if (!(ok = mbar_wait(&bars->q_empty, (q_cnt & 1) ^ 1, abort, status))) break;
+          if (!(ok = mbar_wait<false>(&bars->q_empty, (q_cnt & 1) ^ 1, abort, status))) break;
           mbar_arrive_expect_tx(&bars->q_full, q_bytes);
 #pragma unroll
           for (int c = 0; c < C::KCH; ++c)
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kv = 0; kv < 2; ++kv, ++loads) {
               const int sl = loads % C::SLOTS;
-              if (!(ok = mbar_wait(&bars->ring_empty[sl], ((loads / C::SLOTS) & 1) ^ 1, abort,
+              if (!(ok = mbar_wait<false>(&bars->ring_empty[sl], ((loads / C::SLOTS) & 1) ^ 1, abort,
                                    status)))
                 break;
               uint8_t* dst = smem + C::OFF_RING + sl * C::KV_TILE;
@@ -315,10 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         publish(v);
       }
       // Drain: every copy this thread issued must land before the CTA exits.
-      if (q_cnt) mbar_wait(&bars->q_full, (q_cnt - 1) & 1, abort, status);
+      if (q_cnt) mbar_wait<false>(&bars->q_full, (q_cnt - 1) & 1, abort, status);
       for (int s = 0; s < C::SLOTS; ++s) {
         const uint32_t fills = loads > (uint32_t)s ? (loads - 1 - s) / C::SLOTS + 1 : 0;
-        if (fills) mbar_wait(&bars->ring_full[s], (fills - 1) & 1, abort, status);
+        if (fills) mbar_wait<false>(&bars->ring_full[s], (fills - 1) & 1, abort, status);
       }
     }
   } else if (warp == 1) {
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) mma_commit(bar);
     };
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, status));
+      return __all_sync(0xffffffffu, mbar_wait<false>(bar, parity, abort, status));
     };
     auto wait_slot = [&](uint32_t L) -> bool {
       const bool r = wait(&bars->ring_full[L % C::SLOTS], (L / C::SLOTS) & 1);
@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     while (ok) {
       const int isl = taken % kItemSlots;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->item_full[isl], (taken / kItemSlots) & 1,
+      ok = __all_sync(0xffffffffu, mbar_wait<false>(&bars->item_full[isl], (taken / kItemSlots) & 1,
                                              abort, status));
       if (!ok) break;
       const ItemSlot it = bars->items[isl];
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n; ++j) {
         const uint32_t T_ = gt + j;
         ok = __all_sync(0xffffffffu,
-                        mbar_wait(&bars->s_full[T_ & 1], (T_ >> 1) & 1, abort, status));
+                        mbar_wait<false>(&bars->s_full[T_ & 1], (T_ >> 1) & 1, abort, status));
         if (!ok) break;
         tc_fence_after();
         const uint32_t col_s = C::COL_S + (T_ & 1) * BN;
@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // PV(j-2), so at most PV(j-1) is outstanding and the parity of its
           // phase is unambiguous.  P.V(j) itself needs no wait: it reads the
           // other S buffer and its MMAs follow P.V(j-1) in issue order.
-          ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready, (T_ - 1) & 1, abort, status));
+          ok = __all_sync(0xffffffffu, mbar_wait<false>(&bars->o_ready, (T_ - 1) & 1, abort, status));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
@@ -532,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // epilogue: O / l -> out (rows of this item only)
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done, done & 1, abort, status));
+      ok = __all_sync(0xffffffffu, mbar_wait<false>(&bars->o_done, done & 1, abort, status));
       ++done;
       if (!ok) break;
       tc_fence_after();

@@ -102,14 +102,14 @@ __device__ __forceinline__ int decode_splits(int lkv, int chunk) {
 // shared memory (s_order), so the prefix pass never reads back global memory.
 template <int NT>
 __device__ bool build_list(const AttnParams& p, const SchedConfig& c, const Lengths& seq_lens,
-                           int cls, int chunk, int32_t* order, int32_t* prefix, int* n_out,
-                           int* total_out, unsigned long long* keys, int32_t* s_order,
+                           int cls, int chunk, bool dec_route, int32_t* order, int32_t* prefix,
+                           int* n_out, int* total_out, unsigned long long* keys, int32_t* s_order,
                            long long* scratch) {
   const int B = p.B;
   auto member = [&](int b) -> bool {
     SeqLens s = seq_lens(b);
     if (s.lq <= 0) return false;
-    const bool is_dec = c.decode_enabled && s.lq == 1;
+    const bool is_dec = dec_route && s.lq == 1;
     return cls == 1 ? is_dec : !is_dec;
   };
   auto work = [&](int b) -> long long {
@@ -251,9 +251,18 @@ __global__ void __launch_bounds__(NT) pva_schedule_kernel(AttnParams p, SchedCon
 
   int n_pref = 0, n_items = 0, n_dec = 0, n_units = 0;
   if (s_status == 0) {
+    // Whether single-row sequences go to the split-KV decode kernel (see
+    // SchedConfig::decode_adaptive).
+    bool dec_route = c.decode_enabled != 0;
+    if (dec_route && c.decode_adaptive) {
+      long long single = 0;
+      for (int b = threadIdx.x; b < B; b += NT) single += seq_lens(b).lq == 1;
+      single = block_sum<NT>(single, scratch);
+      dec_route = single * p.Hkv < 2LL * c.num_sms;
+    }
     // Decode chunk: aim for about 8 units per SM, never more partial slots
     // than the workspace holds (all sequences unsplit if it must).
-    if (c.decode_enabled) {
+    if (dec_route) {
       long long keyrows = 0, cnt = 0;
       for (int b = threadIdx.x; b < B; b += NT) {
         SeqLens s = seq_lens(b);
@@ -293,11 +302,11 @@ __global__ void __launch_bounds__(NT) pva_schedule_kernel(AttnParams p, SchedCon
     }
     __syncthreads();
     const int chunk = s_chunk;
-    bool ok = build_list<NT>(p, c, seq_lens, 0, chunk, ws + L.pref_order(), ws + L.pref_prefix(),
-                         &n_pref, &n_items, keys, s_order, scratch);
+    bool ok = build_list<NT>(p, c, seq_lens, 0, chunk, dec_route, ws + L.pref_order(),
+                             ws + L.pref_prefix(), &n_pref, &n_items, keys, s_order, scratch);
     __syncthreads();
-    ok = build_list<NT>(p, c, seq_lens, 1, chunk, ws + L.dec_order(), ws + L.dec_prefix(), &n_dec,
-                    &n_units, keys, s_order, scratch) && ok;
+    ok = build_list<NT>(p, c, seq_lens, 1, chunk, dec_route, ws + L.dec_order(),
+                        ws + L.dec_prefix(), &n_dec, &n_units, keys, s_order, scratch) && ok;
     if (!ok) {
       if (threadIdx.x == 0) atomicOr(&s_status, PVA_DEV_TOO_MANY);
     }
@@ -362,8 +371,12 @@ __global__ void __launch_bounds__(32) pva_schedule_warp_kernel(AttnParams p, Sch
 
   int n_pref = 0, n_items = 0, n_dec = 0, n_units = 0, chunk = INT_MAX;
   if (st == 0) {
-    const bool is_dec = mine && c.decode_enabled && lq == 1;
-    if (c.decode_enabled) {
+    bool dec_route = c.decode_enabled != 0;
+    if (dec_route && c.decode_adaptive)
+      dec_route = (long long)__popc(__ballot_sync(full, mine && lq == 1)) * p.Hkv <
+                  2LL * c.num_sms;
+    const bool is_dec = mine && dec_route && lq == 1;
+    if (dec_route) {
       const long long keyrows = warp_sum_ll(is_dec ? decode_keys(lkv, p.window) : 0) * p.Hkv;
       const long long target = (long long)c.num_sms * 8;
       long long ch = (keyrows + target - 1) / target;

@@ -131,6 +131,21 @@ def test_split_kv_decode_every_shape_and_group(d, dv, G):
     check(out, oracle.attention(q, k, v, cq, ck, G * Hkv, Hkv, 0.0, True, 0.0), "bf16")
 
 
+# Shapes the split-KV kernel serves only for small batches: with single-row
+# sequences x kv heads >= 2 x SMs they go through the tensor-core prefill
+# kernel instead (no key splits), so both routes are checked.
+@pytest.mark.parametrize("d,dv,G,Hkv", [(128, 128, 16, 2), (192, 128, 4, 8), (96, 96, 8, 4)])
+def test_many_single_row_sequences_take_the_prefill_route(d, dv, G, Hkv):
+    B = 200
+    g = torch.Generator().manual_seed(d + G)
+    lkv = torch.randint(1, 700, (B,), generator=g).tolist()
+    q, k, v, cq, ck = workloads.make_packed([1] * B, lkv, G * Hkv, Hkv, d, dv, "bf16", seed=G)
+    words = pva.pva_schedule(cq.to("cuda:0"), ck.to("cuda:0"), B, G * Hkv, Hkv, d, dv, 1, 2)
+    assert words[3] == 0 and words[1] == B  # all routed to the prefill list
+    out = run_gpu(q, k, v, cq, ck, G * Hkv, Hkv, 0.0, True, 0.0)
+    check(out, oracle.attention(q, k, v, cq, ck, G * Hkv, Hkv, 0.0, True, 0.0), "bf16")
+
+
 @pytest.mark.parametrize("d,dv,G,dtype,softcap", [(96, 96, 16, "f16", 0.0),
                                                  (192, 128, 4, "f16", 30.0),
                                                  (128, 128, 16, "bf16", 5.0),
@@ -370,6 +385,9 @@ def sched_mirror(lq, lkv, H, Hkv, d, dtype, num_sms, dv=None):
         paired = d == dv and d in (64, 128)
         tile, units = (128 // G) * (2 if paired else 1), Hkv
         dec = G in (1, 2, 4, 8, 16)
+        tuned = G <= 8 and d == dv and d in (64, 128, 256)
+        if dec and not tuned:  # adaptive: only when too few to fill the SMs
+            dec = sum(1 for a in lq if a == 1) * Hkv < 2 * num_sms
     cap = min(B * Hkv * 16, 16384)
     INT_MAX = 2 ** 31 - 1
     chunk = INT_MAX
@@ -417,7 +435,7 @@ def sched_mirror(lq, lkv, H, Hkv, d, dtype, num_sms, dv=None):
 @pytest.mark.parametrize("seed", range(6))
 @pytest.mark.parametrize("cfg", [(32, 8, 128, 128, 2), (8, 1, 256, 256, 2), (6, 2, 64, 64, 1),
                                  (4, 4, 64, 64, 0), (64, 2, 128, 128, 2), (16, 4, 192, 128, 2),
-                                 (8, 2, 96, 96, 1)])
+                                 (8, 2, 96, 96, 1), (32, 2, 128, 128, 2), (16, 1, 64, 64, 1)])
 def test_scheduler_matches_host_mirror(seed, cfg):
     H, Hkv, d, dv, dtype = cfg
     g = torch.Generator().manual_seed(seed)
@@ -434,7 +452,7 @@ def test_scheduler_matches_host_mirror(seed, cfg):
 
 @pytest.mark.parametrize("B", [1, 2, 7, 31, 32, 33])
 @pytest.mark.parametrize("cfg", [(32, 8, 128, 128, 2), (8, 1, 256, 256, 2), (4, 4, 64, 64, 0),
-                                 (16, 4, 192, 128, 2)])
+                                 (16, 4, 192, 128, 2), (32, 2, 128, 128, 2)])
 def test_scheduler_small_batches_match_host_mirror(B, cfg):
     """B <= 32 runs the one-warp scheduler (33 the CTA one): same words."""
     H, Hkv, d, dv, dtype = cfg
