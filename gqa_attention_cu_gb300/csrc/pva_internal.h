@@ -23,7 +23,8 @@ constexpr int kF32TileTokens = 16;  // query tokens per fp32 work item
 constexpr int kF32KeyTile = 32;     // keys per fp32 key/value tile
 constexpr int kDecodeMaxSplits = 16;
 constexpr int kDecodeMaxGroup = 16;  // largest H/Hkv served by the split-KV decode kernel
-constexpr int kSortMax = 2048;      // sequences sorted on device; more keep input order
+constexpr int kSortMax = 16384;     // sequences sorted on device; more keep input order
+constexpr int kStageMax = 4096;     // sequence lengths staged in shared memory by the scheduler
 
 // Query tiles per prefill work item: two 128-row tiles share each K/V tile
 // in the paired kernel; one tile otherwise (TMEM holds one wide O).

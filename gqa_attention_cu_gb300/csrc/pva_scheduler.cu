@@ -17,8 +17,8 @@
 //     work counters from which the persistent compute kernels draw items.
 //
 // One warp for B <= 32 (everything in registers), else one CTA of 128, 512 or
-// 1024 threads (by B).  B <= 2048 sequences are sorted in shared memory
-// (bitonic); larger batches keep their input order.
+// 1024 threads (by B).  Up to 16384 sequences are sorted in (dynamic) shared
+// memory (bitonic); larger batches keep their input order.
 #include <limits.h>
 
 #include "pva_device.cuh"
@@ -71,7 +71,7 @@ struct SeqLens {
 };
 
 // Per-sequence lengths: from shared memory when the batch was staged there
-// (B <= kSortMax: one coalesced pass over the offsets), else from global.
+// (B <= kStageMax: one coalesced pass over the offsets), else from global.
 struct Lengths {
   const int32_t* cu_q;
   const int32_t* cu_kv;
@@ -98,7 +98,7 @@ __device__ __forceinline__ int decode_splits(int lkv, int chunk) {
 
 // Builds one ordered list (class 0 = prefill, 1 = decode) and its prefix.
 // Returns false when the work count overflows int32.
-// When the batch is staged (B <= kSortMax) the sorted list is also kept in
+// When the batch is sorted (B <= kSortMax) the sorted list is also kept in
 // shared memory (s_order), so the prefix pass never reads back global memory.
 template <int NT>
 __device__ bool build_list(const AttnParams& p, const SchedConfig& c, const Lengths& seq_lens,
@@ -196,11 +196,25 @@ __device__ bool build_list(const AttnParams& p, const SchedConfig& c, const Leng
 
 // NT threads: the smallest of 128, 512, 1024 that covers B (a small batch
 // does not pay for 32 warps walking through every barrier and scan).
+// Dynamic shared memory of the CTA scheduler for a batch of B sequences:
+// sort keys [next power of two >= B] (u64), the sorted list [B], and, for
+// B <= kStageMax, the staged lengths [B] x 2.  Zero when B > kSortMax.
+__host__ __device__ inline size_t sched_smem_bytes(int B) {
+  if (B > kSortMax) return 0;
+  size_t N = 1;
+  while (N < (size_t)B) N <<= 1;
+  return N * 8 + (size_t)B * 4 * (B <= kStageMax ? 3 : 1);
+}
+
 template <int NT>
 __global__ void __launch_bounds__(NT) pva_schedule_kernel(AttnParams p, SchedConfig c) {
-  __shared__ unsigned long long keys[kSortMax];
-  __shared__ int s_lq[kSortMax], s_lkv[kSortMax];
-  __shared__ int32_t s_order[kSortMax];
+  extern __shared__ unsigned long long dyn_smem[];
+  size_t N = 1;
+  while (N < (size_t)p.B) N <<= 1;
+  unsigned long long* keys = dyn_smem;
+  int32_t* s_order = reinterpret_cast<int32_t*>(keys + N);
+  int* s_lq = s_order + p.B;
+  int* s_lkv = s_lq + p.B;
   __shared__ long long scratch[32];
   __shared__ uint32_t s_status;
   __shared__ int s_chunk;
@@ -213,7 +227,7 @@ __global__ void __launch_bounds__(NT) pva_schedule_kernel(AttnParams p, SchedCon
   const WsLayout L{B, p.Hkv};
   int32_t* ws = p.ws;
   SchedHeader* hdr = reinterpret_cast<SchedHeader*>(ws + kWsHeader);
-  const bool staged = B <= kSortMax;
+  const bool staged = B <= kStageMax;
   const Lengths seq_lens{p.cu_q, p.cu_kv, p.kv_len, staged ? s_lq : nullptr,
                          staged ? s_lkv : nullptr};
 
@@ -487,11 +501,17 @@ cudaError_t launch_scheduler(const AttnParams& p, const SchedConfig& c, cudaStre
   if (p.B <= 32)
     pva_schedule_warp_kernel<<<1, 32, 0, s>>>(p, c);
   else if (p.B <= 128)
-    pva_schedule_kernel<128><<<1, 128, 0, s>>>(p, c);
+    pva_schedule_kernel<128><<<1, 128, sched_smem_bytes(p.B), s>>>(p, c);
   else if (p.B <= 512)
-    pva_schedule_kernel<512><<<1, 512, 0, s>>>(p, c);
-  else
-    pva_schedule_kernel<1024><<<1, 1024, 0, s>>>(p, c);
+    pva_schedule_kernel<512><<<1, 512, sched_smem_bytes(p.B), s>>>(p, c);
+  else {
+    // more than 48 KB of dynamic shared memory needs the opt-in
+    cudaError_t e = cudaFuncSetAttribute(pva_schedule_kernel<1024>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sched_smem_bytes(kSortMax));
+    if (e != cudaSuccess) return e;
+    pva_schedule_kernel<1024><<<1, 1024, sched_smem_bytes(p.B), s>>>(p, c);
+  }
   return cudaGetLastError();
 }
 

@@ -415,7 +415,7 @@ def sched_mirror(lq, lkv, H, Hkv, d, dtype, num_sms, dv=None):
         return dec and lq[b] == 1
     pref = [b for b in range(B) if lq[b] > 0 and not is_dec(b)]
     decs = [b for b in range(B) if lq[b] > 0 and is_dec(b)]
-    if B <= 2048:
+    if B <= 16384:
         pref.sort(key=lambda b: (-lkv[b], b))
         decs.sort(key=lambda b: (-lkv[b], b))
 
@@ -467,6 +467,22 @@ def test_scheduler_small_batches_match_host_mirror(B, cfg):
                              workloads.cu_from_lengths(lkv).to(dev), B, H, Hkv, d, dv, 1, dtype)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert words == sched_mirror(lq, lkv, H, Hkv, d, dtype, sms, dv)
+
+
+@pytest.mark.parametrize("B", [2048, 2049, 4096, 9000, 16384, 16385])
+def test_scheduler_large_batches_match_host_mirror(B):
+    """Up to 16384 sequences are sorted longest first on the device (shared
+    memory sized by B); beyond that they keep their input order."""
+    g = torch.Generator().manual_seed(B)
+    lq = torch.randint(0, 64, (B,), generator=g)
+    lq = torch.where(torch.rand(B, generator=g) < 0.5, torch.ones_like(lq), lq).tolist()
+    lkv = (torch.tensor(lq) + torch.randint(0, 3000, (B,), generator=g)).tolist()
+    dev = torch.device("cuda:0")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for H, Hkv, d, dv in ((32, 8, 128, 128), (16, 2, 192, 128)):
+        words = pva.pva_schedule(workloads.cu_from_lengths(lq).to(dev),
+                                 workloads.cu_from_lengths(lkv).to(dev), B, H, Hkv, d, dv, 1, 2)
+        assert words == sched_mirror(lq, lkv, H, Hkv, d, 2, sms, dv)
 
 
 def test_scheduler_configs_match_host_mirror():
