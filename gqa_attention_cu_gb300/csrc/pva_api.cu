@@ -149,6 +149,34 @@ int encode_plane_map(CUtensorMap* map, const void* base, int dtype, int dim, int
   return PVA_OK;
 }
 
+// Rank-4 map over padded slots [slots, rows, heads, dim] (the padded
+// layout of the opset-24 nonpad_kv_seqlen input): boxes of box_rows rows of
+// one kv head of one slot.  Rows outside [0, rows) of a slot read as zeros,
+// so a tile never reaches into the next slot.
+int encode_slot_map(CUtensorMap* map, const void* base, int dtype, int dim, int heads, int rows,
+                    int slots, int box_dim, int box_rows, bool swizzle128) {
+  const cuuint64_t gdim[4] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)rows,
+                              (cuuint64_t)slots};
+  const cuuint64_t gstride[3] = {(cuuint64_t)dim * 2, (cuuint64_t)dim * heads * 2,
+                                 (cuuint64_t)dim * heads * rows * 2};
+  const cuuint32_t box[4] = {(cuuint32_t)box_dim, 1, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  const auto encode = g_encode.load();
+  CUresult r = encode(map, dtype == PVA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                      4, const_cast<void*>(base), gdim, gstride, box, estride,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char msg[160];
+    snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled failed (%d) dim=%d heads=%d rows=%d slots=%d",
+             (int)r, dim, heads, rows, slots);
+    return fail(PVA_ERR_CUDA, msg);
+  }
+  return PVA_OK;
+}
+
 int check_and_plan(const void* q, const void* k, const void* v, const int32_t* cu_q,
                    const int32_t* cu_kv, void* out, int B, int H, int Hkv, int d, int dv,
                    float scale, float softcap, int dtype, Plan* plan) {
@@ -344,6 +372,7 @@ int forward_impl(const Spec& s, void* stream_) {
     p.cu_q = front;
     p.cu_kv = front + B + 1;
     p.kv_len = front + 2 * B + 2;
+    p.kv_slot = s.kv_seq;  // K/V through per-slot maps: padding is never loaded
   }
   if (s.cache) {
     cs = *s.cache;
@@ -389,6 +418,20 @@ int forward_impl(const Spec& s, void* stream_) {
                                    false)) != PVA_OK ||
             (rc = encode_plane_map(&dvm, v, s.dtype, s.dv, cs.cap, planes, s.dv, tkeys,
                                    false)) != PVA_OK)
+          return rc;
+      }
+    } else if (p.kv_slot) {
+      if ((rc = encode_slot_map(&tk, k, s.dtype, s.d, s.Hkv, p.kv_slot, B, 64, bn, true)) !=
+              PVA_OK ||
+          (rc = encode_slot_map(&tv, v, s.dtype, s.dv, s.Hkv, p.kv_slot, B, 64, bn, true)) !=
+              PVA_OK)
+        return rc;
+      if (plan.decode) {
+        const int tkeys = decode_tile_keys(s.d, s.dv);
+        if ((rc = encode_slot_map(&dk, k, s.dtype, s.d, s.Hkv, p.kv_slot, B, s.d, tkeys,
+                                  false)) != PVA_OK ||
+            (rc = encode_slot_map(&dvm, v, s.dtype, s.dv, s.Hkv, p.kv_slot, B, s.dv, tkeys,
+                                  false)) != PVA_OK)
           return rc;
       }
     } else {

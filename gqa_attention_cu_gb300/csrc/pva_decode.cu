@@ -111,15 +111,16 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, const SchedHead
 
 // First row (packed row index) of tile j of a unit.  Packed K/V: tiles are
 // shifted back only at the end of the tensor (rows past the unit are other
-// sequences' keys, weighted 0).  Cache planes: the unit's last tile is shifted
-// back to end at the unit's last key -- before row 0 of the plane, where the
-// tensor copy reads zeros, if the unit is shorter than a tile -- so no row
-// past the sequence's keys, which holds whatever the cache held, is ever
-// loaded.  The rows a shifted tile repeats are masked as already seen.
+// sequences' keys, weighted 0).  Cache planes and padded slots: the unit's
+// last tile is shifted back to end at the unit's last key -- before row 0 of
+// the plane or slot, where the tensor copy reads zeros, if the unit is shorter
+// than a tile -- so no row past the sequence's keys, which holds whatever the
+// cache or the padding held, is ever loaded.  The rows a shifted tile repeats
+// are masked as already seen.
 template <int TK>
 __device__ __forceinline__ int tile_row(const AttnParams& p, const Unit& un, int j,
                                         int total_kv) {
-  const int lim = p.kv_cap ? un.kv_start + un.ke : total_kv;
+  const int lim = p.kv_cap || p.kv_slot ? un.kv_start + un.ke : total_kv;
   return min(un.kv_start + un.ks + j * TK, lim - TK);
 }
 
@@ -247,9 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int k0 = tile_row<TK>(p, un, j, total_kv);
           uint8_t* dk = smem + C::OFF_KV + st * C::STAGE;
           mbar_arrive_expect_tx(&full[st], C::STAGE);
-          const int2 yz = kv_tma_yz(p, un.b, un.g, un.kv_start, k0);
-          tma_load_3d(dk, &tmap_k, &full[st], 0, yz.x, yz.y);
-          tma_load_3d(dk + C::K_BYTES, &tmap_v, &full[st], 0, yz.x, yz.y);
+          load_kv_box(dk, &tmap_k, &full[st], p, 0, un.b, un.g, un.kv_start, k0);
+          load_kv_box(dk + C::K_BYTES, &tmap_v, &full[st], p, 0, un.b, un.g, un.kv_start, k0);
           if (!decoded) {
             nx = decode_unit(p, h, u_next);
             decoded = true;

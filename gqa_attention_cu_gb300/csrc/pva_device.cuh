@@ -226,6 +226,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst_smem, const CUtensorMap* m
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* dst_smem, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst_smem)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // TMA tensor store shared -> global of one box at (x, y, z), tracked by the
 // issuing thread's bulk async-group (commit / wait below).  The x coordinate
 // times the element size must be a multiple of 16 bytes and no coordinate may

@@ -96,6 +96,10 @@ struct AttnParams {
   // rows per (sequence, kv head)) and cu_kv[b] = b * kv_cap; 0: packed
   // [tokens, Hkv, d].
   int kv_cap;
+  // > 0: K and V are padded slots [B, kv_slot, Hkv, d] read through rank-4
+  // tensor maps (dims, kv heads, rows of a slot, slots), so a tile never
+  // crosses into the next slot, and cu_kv[b] = b * kv_slot; 0: rank-3 maps.
+  int kv_slot;
   int B, H, Hkv, G, d, dv;
   float scale;    // resolved (default already applied)
   float softcap;  // 0 = off

@@ -56,22 +56,37 @@ __device__ __forceinline__ int2 kv_tma_yz(const AttnParams& p, int b, int g, int
 }
 
 // Largest token index + 1 a key tile may reach.  Packed tiles are clamped
-// inside the tensor; a cache plane is zero-filled past its capacity by the
-// tensor copy, so cache tiles are never shifted (the host keeps
-// (B + 1) * kv_cap far below INT_MAX).
+// inside the tensor; a cache plane or padded slot is zero-filled past its end
+// by the tensor copy, so those tiles are never shifted for the tensor's sake
+// (the host keeps (B + 1) * kv_cap and B * kv_slot within int32).
 __device__ __forceinline__ int kv_tile_end(const AttnParams& p) {
-  return p.kv_cap ? INT_MAX : p.cu_kv[p.B];
+  return p.kv_cap || p.kv_slot ? INT_MAX : p.cu_kv[p.B];
 }
 
 // End (exclusive packed row) a sequence's key tiles are shifted back to.
-// Packed K/V: the end of the tensor.  Cache planes: the sequence's last key,
-// so that its last tile ends there (starting before row 0, where the tensor
-// copy reads zeros, for a sequence shorter than a tile) and no row past its
-// keys -- whatever the cache holds there -- is ever loaded.  Columns a shifted
+// Packed K/V: the end of the tensor.  Cache planes and padded slots: the
+// sequence's last key, so that its last tile ends there (starting before row
+// 0 of its plane or slot, where the tensor copy reads zeros, for a sequence
+// shorter than a tile) and no row past its keys -- whatever the cache or the
+// padding holds there, NaN included -- is ever loaded.  Columns a shifted
 // tile repeats are masked as already seen.
 __device__ __forceinline__ int key_tile_limit(const AttnParams& p, int kv_start, int lkv,
                                               int total_kv) {
-  return p.kv_cap ? kv_start + lkv : total_kv;
+  return p.kv_cap || p.kv_slot ? kv_start + lkv : total_kv;
+}
+
+// Loads the box of `map` at column x holding key rows [k0, ...) (packed row
+// index) of kv head g of sequence b, whose keys start at packed row
+// kv_start: rank-3 (packed K/V or cache planes) or rank-4 (padded slots).
+__device__ __forceinline__ void load_kv_box(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            const AttnParams& p, int x, int b, int g,
+                                            int kv_start, int k0) {
+  if (p.kv_slot) {
+    tma_load_4d(dst, map, bar, x, g, k0 - kv_start, b);
+  } else {
+    const int2 yz = kv_tma_yz(p, b, g, kv_start, k0);
+    tma_load_3d(dst, map, bar, x, yz.x, yz.y);
+  }
 }
 
 // Row index (in units of head rows) of local key j of kv head g, sequence b.

@@ -283,7 +283,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; ok && j < v.n_tiles; ++j) {
             const int k0 = min(v.kv_start + (v.jb + j) * BN,
                                key_tile_limit(p, v.kv_start, v.lkv, total_kv) - BN);
-            const int2 yz = kv_tma_yz(p, it.b, g, v.kv_start, k0);
 #pragma unroll
             for (int kv = 0; kv < 2; ++kv, ++loads) {
               const int sl = loads % C::SLOTS;
@@ -295,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     (uint32_t)(kv ? C::V_BYTES : C::K_BYTES));
               const int nch = kv ? C::VCH : C::KCH;
               for (int c = 0; c < nch; ++c)
-                tma_load_3d(dst + c * C::KV_CHUNK, kv ? &tmap_v : &tmap_k, &bars->ring_full[sl],
-                            c * 64, yz.x, yz.y);
+                load_kv_box(dst + c * C::KV_CHUNK, kv ? &tmap_v : &tmap_k, &bars->ring_full[sl], p,
+                            c * 64, it.b, g, v.kv_start, k0);
             }
             if (!decoded) {
               it_next = decode_prefill_item(p, h, idx_next);

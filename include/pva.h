@@ -145,11 +145,11 @@ int pva_forward_local(const void* q, const void* k, const void* v,
  *        and `out` is left untouched.
  * B >= 1, q_seq >= 0, kv_seq >= 0, and B * q_seq and B * kv_seq must fit in
  * int32 (else PVA_ERR_INVALID_ARG, nothing enqueued).  The padding rows of k
- * and v are never attended, but they must hold finite values: a key tile that
- * reaches into them multiplies them by zero weights on the tensor cores, and
- * 0 * NaN or 0 * inf is NaN.  The offsets are built on the device by a small
- * kernel in the stream, inside the library's workspace.  Other arguments,
- * errors, memory and asynchrony: as pva_forward.
+ * and v are never read: K and V are loaded through per-slot tensor maps and
+ * each slot's last key tile ends at its last key, so padding may hold
+ * anything, NaN and Inf included.  The offsets are built on the device by a
+ * small kernel in the stream, inside the library's workspace.  Other
+ * arguments, errors, memory and asynchrony: as pva_forward.
  */
 int pva_forward_padded(const void* q, const void* k, const void* v,
                        const int64_t* nonpad_kv_seqlen, void* out, int B, int q_seq,

@@ -4,9 +4,10 @@ The opset-24 Attention input ``nonpad_kv_seqlen`` (attention.rs: per-batch
 causal offset nonpad[b] - q_seq and padding frontier j >= nonpad[b]; the
 packed_varlen_attention.rs module doc relates it to the packed op through the
 exclusive prefix sum).  Each case runs the CUDA path on the padded tensors --
-whose padding rows hold large finite values that would wreck any output
-attending them -- and compares it with ``oracle.attention_padded`` element by
-element; one case also checks the packed entry point on the same rows.
+whose padding rows hold values that would wreck any output attending them --
+and compares it with ``oracle.attention_padded`` element by element; one case
+also checks the packed entry point on the same rows, and one that NaN or Inf
+padding changes no output bit.
 """
 import numpy as np
 import pytest
@@ -90,6 +91,36 @@ def test_padding_contents_do_not_change_a_bit(q_seq, causal):
     for pad in ((0.0, 0.0), (60.0, -300.0), (-1e4, 3e4)):
         q, k, v, npd = padded_inputs(*args, seed=8, pad=pad)
         outs.append(run_padded(q, k, v, npd, 16, 4, 0.0, causal, softcap=30.0))
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+@pytest.mark.parametrize("q_seq,kv_seq,H,Hkv,d,dv,dtype", [
+    (1, 3000, 32, 8, 128, 128, "bf16"),   # split-KV decode
+    (1, 700, 8, 1, 256, 256, "bf16"),
+    (1, 40, 16, 2, 192, 128, "bf16"),     # decode, slots shorter than a tile
+    (300, 900, 16, 4, 128, 128, "bf16"),  # paired prefill
+    (129, 5, 8, 2, 64, 64, "f16"),        # paired prefill, 5-row slots
+    (200, 640, 8, 1, 256, 256, "bf16"),   # single-tile prefill
+    (130, 300, 16, 4, 192, 128, "bf16"),
+    (17, 90, 4, 2, 64, 48, "f32"),        # fp32 kernel
+])
+def test_nan_and_inf_padding_give_the_outputs_of_zero_padding(q_seq, kv_seq, H, Hkv, d, dv,
+                                                             dtype):
+    """No kernel ever loads a row past nonpad[b]: the last key tile of each
+    slot ends at its last key, so padding may hold anything -- NaN and Inf
+    included -- and the outputs are bit for bit those of zero padding."""
+    nonpad = [kv_seq, 1, 0, max(1, kv_seq // 3), max(1, kv_seq - 7)]
+    B = len(nonpad)
+    causal = q_seq != 129
+    outs = []
+    for pad in ((0.0, 0.0), (float("nan"), float("nan")), (float("inf"), float("-inf"))):
+        q, k, v, npd = padded_inputs(B, q_seq, kv_seq, nonpad, H, Hkv, d, dv, dtype, seed=9,
+                                     pad=pad)
+        outs.append(run_padded(q, k, v, npd, H, Hkv, 0.0, causal, softcap=20.0))
+    ref = oracle.attention_padded(*padded_inputs(B, q_seq, kv_seq, nonpad, H, Hkv, d, dv, dtype,
+                                                 seed=9, pad=(0.0, 0.0))[:4], H, Hkv, 0.0,
+                                  causal, 20.0)
+    check(outs[0], ref, dtype)
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
