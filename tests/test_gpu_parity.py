@@ -249,6 +249,28 @@ def test_softcap_bf16_with_large_scores():
            seed=26)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+def test_running_maximum_growing_across_and_within_key_tiles(d, causal):
+    """Keys grow along each sequence, most in the second half of every 128-key
+    tile, so the row maximum rises by more than the rescale threshold after
+    a sequence's first key tile, also between the two halves of a tile: the
+    paths that rescale O in the middle of an item."""
+    lq, lkv = [700, 300, 129], [700, 460, 129]
+    q, k, v, cq, ck = workloads.make_packed(lq, lkv, 8, 2, d, d, "bf16", seed=d + int(causal))
+    kf = k.float()
+    for b in range(len(lkv)):
+        j = torch.arange(lkv[b], dtype=torch.float32)
+        grow = 1.0 + j / 48.0 + 3.0 * ((j % 128) >= 64).float() * (j >= 128).float()
+        kf[int(ck[b]):int(ck[b + 1])] *= grow[:, None, None]
+    k = kf.to(torch.bfloat16)
+    # the softmax is sharply peaked here (outputs near single V rows): V at
+    # half scale keeps the outputs within the magnitudes the bf16 bound is for
+    v = (v.float() * 0.5).to(torch.bfloat16)
+    out = run_gpu(q, k, v, cq, ck, 8, 2, 0.0, causal, 0.0)
+    check(out, oracle.attention(q, k, v, cq, ck, 8, 2, 0.0, causal, 0.0), "bf16")
+
+
 def test_explicit_scale():
     parity([64, 10], [64, 90], 4, 4, 64, "bf16", causal=False, scale=0.05, seed=27)
 
