@@ -18,21 +18,33 @@
 // Per CTA (persistent, one per SM, 192 threads):
 //   warp 0      TMA producer: draws work items from a device-wide counter,
 //               publishes each decoded item through a shared-memory ring, and
-//               loads the Q tile, then K_j and V_j into a 5-slot ring.
-//   warp 1      MMA issuer + TMEM owner.  S is double-buffered in TMEM
-//               (S(j) in buffer j & 1), so S(j+1) runs while tile j is being
+//               loads the Q tile, then K_j and V_j, into one ring of 7 or 8
+//               slots (the Q tile takes 2 or 3 slots).
+//   warp 1      MMA issuer + TMEM owner.  S = Q K^T takes Q from TMEM and K
+//               from shared memory, so each S MMA reads only its 64 K rows
+//               from shared memory.  S is double-buffered in TMEM (S(j) in
+//               buffer j & 1), so S(j+1) runs while tile j is being
 //               exponentiated; P(j) (16-bit pairs) overwrites S(j)'s buffer and
 //               feeds O += P V with A taken from TMEM; S(j+2) reuses the buffer
 //               after that MMA (tcgen05 MMAs of one thread run in issue order).
-//   warps 2..5  softmax / correction / epilogue, one thread per TMEM lane.
-// TMEM: S buffers [0,64) and [64,128), O [128,128+dv).  Shared memory (d = dv
-// = 256): Q 64 KB + 5 K/V slots of 32 KB (more, smaller slots at d < 256).
+//   warps 2..5  softmax / correction / epilogue, one thread per TMEM lane;
+//               they also move each Q tile from its ring slots into TMEM,
+//               the next item's before the current item's epilogue.
+// TMEM: S buffers [0,64) and [64,128), O [128,128+dv), Q [128+dv,
+// 128+dv+d/2) (512 columns at d = dv = 256).
 //
 // Softcap: tanh(t) of the scaled score t = s * scale / softcap comes from its
-// Maclaurin series t - t^3/3 + 2t^5/15 - 17t^7/315 + 62t^9/2835 -
-// 1382t^11/155925 (error < 4e-7 for |t| <= 1/2) on the FMA pipe whenever every
-// score of the warp's tile has |t| <= 1/2; otherwise from the identity
+// Maclaurin series t - t^3/3 + 2t^5/15 (error < 3.3e-6 for |t| <= 1/4, i.e.
+// below 2.4e-4 in the base-2 exponent at softcap 50) with the softcap folded
+// into the coefficients, on the FMA pipe, whenever every score of the warp's
+// tile has |t| <= 1/4; otherwise from the identity
 // tanh(t) = 1 - 2 / (exp(2t) + 1).
+//
+// Key tiles that no row of a warp masks, after the rows' first visible tile,
+// are exponentiated in one pass against the running maximum; the pass also
+// finds the largest exponent (and series argument), and the rare tile that
+// would need a larger maximum (or leaves the series range) is redone with
+// the maximum taken first.
 #include "pva_device.cuh"
 #include "pva_items.cuh"
 
@@ -44,34 +56,40 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows > 2^8
 constexpr int kItemSlots = 4;
 constexpr int kSoftmaxWarps = 4;
-constexpr float kPolyLimit = 0.5f;          // |t| range of the tanh series
+constexpr float kPolyLimit = 0.25f;         // |t| range of the tanh series
 
 template <int DQK, int DV>
 struct TcCfg {
-  static_assert(DQK % 16 == 0 && DV % 32 == 0 && DQK <= 256 && DV <= 256, "head sizes");
+  static_assert(DQK % 32 == 0 && DV % 32 == 0 && DQK <= 256 && DV <= 256, "head sizes");
   static constexpr int BN = 64;
   static constexpr int KCH = (DQK + 63) / 64;     // 128-byte column chunks of a q/k row
   static constexpr int VCH = (DV + 63) / 64;      // the same for a v row
   static constexpr int Q_CHUNK = kTcRows * 128;   // bytes of one chunk of the Q tile
-  static constexpr int Q_BYTES = KCH * Q_CHUNK;
   static constexpr int KV_CHUNK = BN * 128;       // bytes of one chunk of a K or V tile
   static constexpr int K_BYTES = KCH * KV_CHUNK;
   static constexpr int V_BYTES = VCH * KV_CHUNK;
   static constexpr int KV_TILE = K_BYTES > V_BYTES ? K_BYTES : V_BYTES;  // one ring slot
-  // As many K/V slots as shared memory holds next to Q (at most 8): 5 at
-  // d = 256, 7 at d = 192, 8 at d = 96.  A deeper ring starts each load
-  // earlier before its tile is needed.
-  static constexpr int SLOTS_FIT = (232448 - 64 - 2048 - Q_BYTES) / KV_TILE;
+  // The Q tile passes through the K/V ring on its way to TMEM: Q_PER_SLOT of
+  // its 64-column chunks per slot, Q_SLOTS slots per tile.
+  static constexpr int Q_PER_SLOT = KV_TILE / Q_CHUNK;
+  static_assert(Q_PER_SLOT >= 1, "a Q chunk fits a ring slot");
+  static constexpr int Q_SLOTS = (KCH + Q_PER_SLOT - 1) / Q_PER_SLOT;
+  // As many ring slots as shared memory holds (at most 8): 7 at d = 256, 8
+  // at d = 192 and d = 96.  A deeper ring starts each load earlier before
+  // its tile is needed.
+  static constexpr int SLOTS_FIT = (232448 - 64 - 2048) / KV_TILE;
   static constexpr int SLOTS = SLOTS_FIT < 8 ? SLOTS_FIT : 8;
-  static_assert(SLOTS >= 4, "K/V ring depth");
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_RING = Q_BYTES;
+  static_assert(SLOTS >= Q_SLOTS + 2, "K/V ring depth");
+  static constexpr int OFF_RING = 0;
   static constexpr int OFF_BAR = OFF_RING + SLOTS * KV_TILE;
   static constexpr int SMEM = OFF_BAR + 1024 + 1024;  // barriers/items + alignment slack
   static constexpr int TMEM_COLS = 512;
   static constexpr int COL_S = 0;                 // + BN * buffer
   static constexpr int COL_O = 2 * BN;
-  static_assert(2 * BN + DV <= TMEM_COLS, "TMEM budget");
+  // Q as the A operand of S = Q K^T: row r in lane r, dims (2c, 2c+1) as a
+  // 16-bit pair in column COL_Q + c
+  static constexpr int COL_Q = COL_O + DV;
+  static_assert(COL_Q + DQK / 2 <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448 - 64, "shared memory budget");
 };
 
@@ -84,7 +102,7 @@ struct ItemSlot {
 };
 
 struct Bars {
-  uint64_t q_full, q_empty, o_ready, o_done, o_free, drain;
+  uint64_t q_tmem, o_ready, o_done, o_free, drain;
   uint64_t s_full[2], p_full[2];
   uint64_t ring_full[8], ring_empty[8];
   uint64_t item_full[kItemSlots], item_empty[kItemSlots];
@@ -115,30 +133,27 @@ __device__ __forceinline__ void extremes64(const uint32_t (&va)[32], const uint3
   mn = fminf(b[0], b[1]);
 }
 
-// tanh(t) for |t| <= 1/2 from its Maclaurin series through t^11 (Horner in
-// t^2; truncation error below 4e-7), on a pair of scores with packed f32x2
-// FMAs (a product is an FMA with a zero addend): half the instructions of
-// the scalar chain, the same rounded operations in each lane.
-__device__ __forceinline__ float2 tanh_series2(float2 t) {
-  const float2 z = make_float2(0.0f, 0.0f);
-  const float2 u = ffma2(t, t, z);
-  float2 p = make_float2(-0.008863235529902197f, -0.008863235529902197f);
-  p = ffma2(p, u, make_float2(0.021869488536155203f, 0.021869488536155203f));
-  p = ffma2(p, u, make_float2(-0.05396825396825397f, -0.05396825396825397f));
-  p = ffma2(p, u, make_float2(0.13333333333333333f, 0.13333333333333333f));
-  p = ffma2(p, u, make_float2(-0.3333333333333333f, -0.3333333333333333f));
-  p = ffma2(p, u, make_float2(1.0f, 1.0f));
-  return ffma2(t, p, z);
-}
-
-// 2^(x - m) over the 64 columns, row sum, P packed as 16-bit pairs.
-// MODE 0: no softcap; 1: softcap via the series; 2: softcap via exp/rcp.
-template <typename T, int MODE, bool MASKED>
+// 2^(x - m) over the 64 columns, row sum, P packed as 16-bit pairs, where x
+// is the scaled (MODE 0) or softcapped score in base-2 units.  MODE 1: A *
+// tanh(u) for |u| <= 1/4 from the first three terms of the tanh series,
+// u - u^3/3 + 2u^5/15, with A folded into the coefficients (u * (A + w *
+// (-A/3 + w * 2A/15)), w = u^2); the series alternates with falling terms,
+// so the error is below the next one, 17/315 |u|^7 < 3.3e-6.  MODE 2: tanh
+// from exp/rcp.  TRACK also returns the largest x - m and (MODE 1) the
+// largest w, with which a caller checks a guessed m and the series range
+// after the fact.
+template <typename T, int MODE, bool MASKED, bool TRACK = false>
 __device__ __forceinline__ float exp64(const uint32_t (&va)[32], const uint32_t (&vb)[32],
                                        int lo_c, int hi_c, float s_mul, float cap_mul,
-                                       float m_eff, uint32_t (&pw)[32]) {
+                                       float m_eff, uint32_t (&pw)[32], float* xmax = nullptr,
+                                       float* wmax = nullptr) {
+  const float2 z = make_float2(0.0f, 0.0f);
   const float2 mul2 = make_float2(s_mul, s_mul), neg_m = make_float2(-m_eff, -m_eff);
-  float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+  const float2 a2 = make_float2(cap_mul, cap_mul);
+  const float2 c1 = make_float2(cap_mul * (-1.0f / 3.0f), cap_mul * (-1.0f / 3.0f));
+  const float2 c2 = make_float2(cap_mul * (2.0f / 15.0f), cap_mul * (2.0f / 15.0f));
+  float2 acc[2] = {z, z};
+  float xm[2] = {__int_as_float(0xff800000), __int_as_float(0xff800000)}, wm[2] = {0.0f, 0.0f};
 #pragma unroll
   for (int e = 0; e < 64; e += 2) {
     const float2 s = make_float2(col32(va, vb, e), col32(va, vb, e + 1));
@@ -146,8 +161,10 @@ __device__ __forceinline__ float exp64(const uint32_t (&va)[32], const uint32_t 
     if (MODE == 0) {
       x = ffma2(s, mul2, neg_m);
     } else if (MODE == 1) {
-      const float2 z = make_float2(0.0f, 0.0f), cap2 = make_float2(cap_mul, cap_mul);
-      x = ffma2(cap2, tanh_series2(ffma2(s, mul2, z)), neg_m);
+      const float2 u = ffma2(s, mul2, z);
+      const float2 w = ffma2(u, u, z);
+      x = ffma2(u, ffma2(w, ffma2(w, c2, c1), a2), neg_m);
+      if (TRACK) wm[(e >> 1) & 1] = fmax3f(wm[(e >> 1) & 1], w.x, w.y);
     } else {
       x.x = fmaf(cap_mul, tanh_via_exp2(s.x * s_mul), -m_eff);
       x.y = fmaf(cap_mul, tanh_via_exp2(s.y * s_mul), -m_eff);
@@ -157,9 +174,14 @@ __device__ __forceinline__ float exp64(const uint32_t (&va)[32], const uint32_t 
       x.x = (e >= lo_c && e < hi_c) ? x.x : ninf;
       x.y = (e + 1 >= lo_c && e + 1 < hi_c) ? x.y : ninf;
     }
+    if (TRACK) xm[(e >> 1) & 1] = fmax3f(xm[(e >> 1) & 1], x.x, x.y);
     const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
     acc[(e >> 1) & 1] = fadd2(acc[(e >> 1) & 1], p);
     pw[e >> 1] = pack2<T>(p.x, p.y);
+  }
+  if (TRACK) {
+    *xmax = fmaxf(xm[0], xm[1]);
+    if (MODE == 1) *wmax = fmaxf(wm[0], wm[1]);
   }
   const float2 r = fadd2(acc[0], acc[1]);
   return r.x + r.y;
@@ -175,7 +197,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sQ = smem + C::OFF_Q;
   Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
@@ -190,15 +211,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     s_abort = 0;
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->q_tmem, 32 * kSoftmaxWarps);
     mbar_init(&bars->o_ready, 1);
     mbar_init(&bars->o_done, 1);
-    mbar_init(&bars->o_free, 128);
+    mbar_init(&bars->o_free, 32 * kSoftmaxWarps);
     mbar_init(&bars->drain, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->p_full[b], 128);
+      mbar_init(&bars->p_full[b], 32 * kSoftmaxWarps);
     }
     for (int s = 0; s < C::SLOTS; ++s) {
       mbar_init(&bars->ring_full[s], 1);
@@ -210,11 +230,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
   }
-  // Rows of the Q tile beyond G*m are never written by the TMA unit; start
-  // them from zeros so no stale bits reach the MMA.
-  for (int i = threadIdx.x; i < C::Q_BYTES / 16; i += kThreads)
-    reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
-  fence_proxy_async_smem();
   if (warp == 1) tmem_alloc<C::TMEM_COLS>(&s_tmem_base);
   if (warp == 0 && lane == 0) {
     prefetch_tensor_map(&tmap_q);
@@ -232,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const SchedHeader h = *reinterpret_cast<const SchedHeader*>(p.ws + kWsHeader);
-      uint32_t q_cnt = 0, loads = 0, published = 0;
-      const uint32_t q_bytes = (uint32_t)C::KCH * (uint32_t)(G * m_tok) * 128u;
+      uint32_t loads = 0, published = 0;
+      const uint32_t q_chunk_bytes = (uint32_t)(G * m_tok) * 128u;
       bool ok = true;
       auto publish = [&](const ItemSlot& v) -> bool {
         const int sl = published % kItemSlots;
@@ -274,12 +289,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = publish(v))) break;
         if (v.n_tiles > 0) {
           const int g = v.unit;
-          if (!(ok = mbar_wait<false>(&bars->q_empty, (q_cnt & 1) ^ 1, abort, status))) break;
-          mbar_arrive_expect_tx(&bars->q_full, q_bytes);
-#pragma unroll
-          for (int c = 0; c < C::KCH; ++c)
-            tma_load_3d(sQ + c * C::Q_CHUNK, &tmap_q, &bars->q_full, c * 64, g * G, v.q0);
-          ++q_cnt;
+          // the Q tile: Q_PER_SLOT chunks in each of the next Q_SLOTS slots
+          for (int qs = 0; ok && qs < C::Q_SLOTS; ++qs, ++loads) {
+            const int sl = loads % C::SLOTS;
+            if (!(ok = mbar_wait<false>(&bars->ring_empty[sl], ((loads / C::SLOTS) & 1) ^ 1, abort,
+                                        status)))
+              break;
+            const int c_lo = qs * C::Q_PER_SLOT, c_hi = min(C::KCH, c_lo + C::Q_PER_SLOT);
+            mbar_arrive_expect_tx(&bars->ring_full[sl], (uint32_t)(c_hi - c_lo) * q_chunk_bytes);
+            for (int c = c_lo; c < c_hi; ++c)
+              tma_load_3d(smem + C::OFF_RING + sl * C::KV_TILE + (c - c_lo) * C::Q_CHUNK, &tmap_q,
+                          &bars->ring_full[sl], c * 64, g * G, v.q0);
+          }
           for (int j = 0; ok && j < v.n_tiles; ++j) {
             const int k0 = min(v.kv_start + (v.jb + j) * BN,
                                key_tile_limit(p, v.kv_start, v.lkv, total_kv) - BN);
@@ -314,7 +335,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         publish(v);
       }
       // Drain: every copy this thread issued must land before the CTA exits.
-      if (q_cnt) mbar_wait<false>(&bars->q_full, (q_cnt - 1) & 1, abort, status);
       for (int s = 0; s < C::SLOTS; ++s) {
         const uint32_t fills = loads > (uint32_t)s ? (loads - 1 - s) / C::SLOTS + 1 : 0;
         if (fills) mbar_wait<false>(&bars->ring_full[s], (fills - 1) & 1, abort, status);
@@ -327,10 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_s = idesc_f16<T>(kTcRows, BN, false, false);
     constexpr uint32_t idesc_o = idesc_f16<T>(kTcRows, DV, false, true);
     // Base descriptors, built once: the issue loops only add constants.
-    const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t kdesc = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
     const uint64_t vdesc = sdesc_sw128(smem_u32(smem + C::OFF_RING), C::KV_CHUNK, 1024);
-    uint32_t q_cnt = 0, loads = 0, gt = 0, items = 0, taken = 0;
+    uint32_t q_cnt = 0, loads = 0, gt = 0, items = 0, taken = 0;  // q_cnt: Q tiles in TMEM
     bool ok = true;
     auto commit = [&](uint64_t* bar) {
       if (leader) mma_commit(bar);
@@ -350,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;
-          mma_ss(tmem + C::COL_S + (T_ & 1) * BN, sdesc_advance(qdesc, (kk >> 2) * C::Q_CHUNK + off),
+          mma_ts(tmem + C::COL_S + (T_ & 1) * BN, tmem + C::COL_Q + kk * 8,
                  sdesc_advance(ka, (kk >> 2) * C::KV_CHUNK + off), idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->s_full[T_ & 1]);
@@ -366,15 +385,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++taken;
       if (last) break;
       if (n == 0) continue;
-      if (!(ok = wait(&bars->q_full, q_cnt & 1))) break;
+      // Q is in TMEM once every softmax thread has copied its share; its
+      // ring slots are free from then on.
+      if (!(ok = wait(&bars->q_tmem, q_cnt & 1))) break;
       tc_fence_after();
+      if (leader) {
+        for (int qs = 0; qs < C::Q_SLOTS; ++qs) mbar_arrive(&bars->ring_empty[(loads + qs) % C::SLOTS]);
+      }
+      loads += C::Q_SLOTS;
       // key tile j: K in load slot loads + 2j, V in loads + 2j + 1
       for (int j = 0; ok && j < 2 && j < n; ++j) {
         if (!(ok = wait_slot(loads + 2 * j))) break;
         issue_s(gt + j, loads + 2 * j);
       }
       if (!ok) break;
-      if (n <= 2) commit(&bars->q_empty);
       for (int j = 0; ok && j < n; ++j) {
         const uint32_t T_ = gt + j, Lv = loads + 2 * j + 1;
         // P.V(j) needs V_j and P(j) only.  K_{j+2} is waited for only after
@@ -400,7 +424,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j + 2 < n) {
           if (!(ok = wait_slot(loads + 2 * (j + 2)))) break;
           issue_s(T_ + 2, loads + 2 * (j + 2));
-          if (j + 3 == n) commit(&bars->q_empty);
         }
       }
       loads += 2 * n;
@@ -413,6 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     wait(&bars->drain, 0);
   } else {
     // ------------------------------------------------- softmax + epilogue
+    // One thread per TMEM lane (query row).  These warps also move each Q
+    // tile from its ring slots into TMEM, the next item's before the current
+    // item's epilogue.
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int r = quarter * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
@@ -421,8 +447,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float cap_mul = p.softcap * kLog2e;
     const bool up = p.scale > 0.0f;  // direction of the (monotone) score transform
     uint32_t gt = 0, taken = 0, done = 0;  // done: items with key tiles
-    bool ok = true;
+    uint32_t lq = 0;  // ring loads accounted for (the producer's order)
+    bool ok = true, q_pre = false;  // q_pre: the next item's Q is in TMEM
     T* out = static_cast<T*>(p.out);
+    const int rows = G * m_tok;  // rows of the Q tile the TMA unit writes
+    // Copies the next Q tile from its ring slots into TMEM (rows beyond the
+    // tile as zeros) and signals the MMA warp.  Every S MMA of the previous
+    // item has completed: its last S tile was waited for.
+    auto copy_q = [&]() -> bool {
+      bool got = true;
+      for (int qs = 0; qs < C::Q_SLOTS; ++qs) {
+        const uint32_t L = lq + qs;
+        got = got && mbar_wait<false>(&bars->ring_full[L % C::SLOTS], (L / C::SLOTS) & 1, abort,
+                                      status);
+      }
+      if (!__all_sync(0xffffffffu, got)) return false;
+#pragma unroll 1
+      for (int c = 0; c < C::KCH; ++c) {
+        const uint32_t L = lq + c / C::Q_PER_SLOT;
+        const uint8_t* src = smem + C::OFF_RING + (L % C::SLOTS) * C::KV_TILE +
+                             (c % C::Q_PER_SLOT) * C::Q_CHUNK + r * 128;
+        uint32_t w[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {  // 16-byte unit u of the row, 128-byte swizzle
+          uint4 x = make_uint4(0, 0, 0, 0);
+          if (r < rows) x = *reinterpret_cast<const uint4*>(src + ((u ^ (r & 7)) << 4));
+          w[4 * u] = x.x;
+          w[4 * u + 1] = x.y;
+          w[4 * u + 2] = x.z;
+          w[4 * u + 3] = x.w;
+        }
+        if (DQK % 64 == 0 || c + 1 < C::KCH) {
+          tmem_st32(t_lane + C::COL_Q + c * 32, w);
+        } else {  // a 32-column tail chunk
+          uint32_t w16[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w16[e] = w[e];
+          tmem_st16(t_lane + C::COL_Q + c * 32, w16);
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();  // the slots are refilled by the TMA unit next
+      tc_fence_before();
+      mbar_arrive(&bars->q_tmem);
+      lq += C::Q_SLOTS;
+      return true;
+    };
 
     while (ok) {
       const int isl = taken % kItemSlots;
@@ -448,6 +518,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
+      if (!q_pre && !(ok = copy_q())) break;
+      q_pre = false;
+      lq += 2 * n;
       const int off = it.lkv - it.lq;
       const int row_hi = p.is_causal ? min(it.lkv, i + off + 1) : it.lkv;
       const int row_lo = p.window > 0 ? i + off + 1 - p.window : 0;  // local window start
@@ -471,37 +544,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lo_c = max(J * BN, row_lo) - base;  // visible columns [lo_c, hi_c)
         const int hi_c = min((J + 1) * BN, row_hi) - base;
         const bool masked = !__all_sync(0xffffffffu, lo_c <= 0 && hi_c >= BN);
-        float mx, mn;
-        if (masked)
-          extremes64<true>(va, vb, lo_c, hi_c, mx, mn);
-        else
-          extremes64<false>(va, vb, lo_c, hi_c, mx, mn);
-        const float ext = up ? mx : mn;  // the transform is monotone in the raw score
-        const bool any = mx != NEG_INF;
-        float mt = NEG_INF;
-        if (any) mt = CAP ? cap_mul * tanh_via_exp2(ext * s_mul) : ext * s_mul;
-        const float m_new = fmaxf(m_used, mt);
-        float alpha = 1.0f;
-        if (m_new > m_used + kRescaleThreshold) {
-          alpha = ex2_approx(m_used - m_new);  // 0 when m_used is -inf
-          m_used = m_new;
-        }
-        const float m_eff = m_used == NEG_INF ? 0.0f : m_used;
         uint32_t pw[32];
-        float rs;
-        if (!CAP) {
-          rs = masked ? exp64<T, 0, true>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw)
-                      : exp64<T, 0, false>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw);
-        } else {
-          // every visible score of the warp has |t| <= 1/2: tanh from its series
-          const float tmax = fmaxf(fabsf(mx * s_mul), fabsf(mn * s_mul));
-          const bool series = __all_sync(0xffffffffu, !any || tmax <= kPolyLimit);
-          if (series)
-            rs = masked ? exp64<T, 1, true>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw)
-                        : exp64<T, 1, false>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw);
+        float rs, alpha = 1.0f;
+        // An unmasked tile after the row's first visible one is exponentiated
+        // once against the running maximum m, tracking the largest exponent
+        // (and, with a softcap, the series argument): the maximum only has
+        // to be raised when an exponent exceeds the rescale threshold, which
+        // after the first tiles is rare.  Then, or when the series range is
+        // left, the tile is redone as below.
+        bool redo = masked || !__all_sync(0xffffffffu, m_used != NEG_INF);
+        if (!redo) {
+          float xm, wm = 0.0f;
+          if (!CAP)
+            rs = exp64<T, 0, false, true>(va, vb, 0, BN, s_mul, cap_mul, m_used, pw, &xm);
           else
-            rs = masked ? exp64<T, 2, true>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw)
-                        : exp64<T, 2, false>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw);
+            rs = exp64<T, 1, false, true>(va, vb, 0, BN, s_mul, cap_mul, m_used, pw, &xm, &wm);
+          redo = __any_sync(0xffffffffu,
+                            xm > kRescaleThreshold || (CAP && wm > kPolyLimit * kPolyLimit));
+        }
+        if (redo) {
+          float mx, mn;
+          if (masked)
+            extremes64<true>(va, vb, lo_c, hi_c, mx, mn);
+          else
+            extremes64<false>(va, vb, lo_c, hi_c, mx, mn);
+          const float ext = up ? mx : mn;  // the transform is monotone in the raw score
+          const bool any = mx != NEG_INF;
+          float mt = NEG_INF;
+          if (any) mt = CAP ? cap_mul * tanh_via_exp2(ext * s_mul) : ext * s_mul;
+          const float m_new = fmaxf(m_used, mt);
+          if (m_new > m_used + kRescaleThreshold) {
+            alpha = ex2_approx(m_used - m_new);  // 0 when m_used is -inf
+            m_used = m_new;
+          }
+          const float m_eff = m_used == NEG_INF ? 0.0f : m_used;
+          if (!CAP) {
+            rs = masked ? exp64<T, 0, true>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw)
+                        : exp64<T, 0, false>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw);
+          } else {
+            // every visible score of the warp has |t| <= 1/4: tanh from its series
+            const float tmax = fmaxf(fabsf(mx * s_mul), fabsf(mn * s_mul));
+            const bool series = __all_sync(0xffffffffu, !any || tmax <= kPolyLimit);
+            if (series)
+              rs = masked ? exp64<T, 1, true>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw)
+                          : exp64<T, 1, false>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw);
+            else
+              rs = masked ? exp64<T, 2, true>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw)
+                          : exp64<T, 2, false>(va, vb, lo_c, hi_c, s_mul, cap_mul, m_eff, pw);
+          }
         }
         // P (16-bit pairs) over the S buffer's first 32 columns
         tmem_st32(t_lane + col_s, pw);
@@ -529,6 +619,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars->p_full[T_ & 1]);
       }
       if (!ok) break;
+
+      // The next item's Q goes to TMEM before this item's epilogue, so that
+      // its first S MMAs run meanwhile.
+      {
+        const int nsl = taken % kItemSlots;
+        ok = __all_sync(0xffffffffu, mbar_wait<false>(&bars->item_full[nsl],
+                                                      (taken / kItemSlots) & 1, abort, status));
+        if (!ok) break;
+        const ItemSlot nx = bars->items[nsl];
+        if (!nx.last && nx.n_tiles > 0) {
+          if (!(ok = copy_q())) break;
+          q_pre = true;
+        }
+      }
 
       // epilogue: O / l -> out (rows of this item only)
       ok = __all_sync(0xffffffffu, mbar_wait<false>(&bars->o_done, done & 1, abort, status));
