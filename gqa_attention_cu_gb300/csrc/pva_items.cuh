@@ -26,8 +26,14 @@ __device__ __forceinline__ int find_segment(const int32_t* prefix, int n, int it
   return lo;
 }
 
+// Item `it` of the longest-first list: the sequences in pref_order, each
+// contributing (query tiles x units) items.  Within a sequence the default
+// order is query tile major (latest, most expensive tile first, all units of
+// it); unit_major walks one unit's tiles after another instead, which keeps
+// the K/V of few units hot in L2 when every unit has its own K/V (G = 1).
 __device__ __forceinline__ PrefillItem decode_prefill_item(const AttnParams& p,
-                                                           const SchedHeader& h, int it) {
+                                                           const SchedHeader& h, int it,
+                                                           bool unit_major = false) {
   const WsLayout L{p.B, p.Hkv};
   const int32_t* order = p.ws + L.pref_order();
   const int32_t* prefix = p.ws + L.pref_prefix();
@@ -41,9 +47,16 @@ __device__ __forceinline__ PrefillItem decode_prefill_item(const AttnParams& p,
   r.lq = p.cu_q[r.b + 1] - r.q_start;
   r.lkv = p.kv_len ? p.kv_len[r.b] : p.cu_kv[r.b + 1] - r.kv_start;
   const int n_tiles = (r.lq + h.tile_tokens - 1) / h.tile_tokens;
-  const int rank = local / h.units_per_tile;
-  r.unit = local - rank * h.units_per_tile;
-  r.t = n_tiles - 1 - rank;  // most expensive (latest) query tile first
+  if (unit_major) {
+    // one unit's query tiles after another (latest first within each), so
+    // that the CTAs running at the same time read the same unit's K/V
+    r.unit = local / n_tiles;
+    r.t = n_tiles - 1 - (local - r.unit * n_tiles);
+  } else {
+    const int rank = local / h.units_per_tile;
+    r.unit = local - rank * h.units_per_tile;
+    r.t = n_tiles - 1 - rank;  // most expensive (latest) query tile first
+  }
   return r;
 }
 

@@ -18,7 +18,7 @@
 // Per CTA (persistent, one per SM, 192 threads):
 //   warp 0      TMA producer: draws work items from a device-wide counter,
 //               publishes each decoded item through a shared-memory ring, and
-//               loads the Q tile, then K_j and V_j, into one ring of 7 or 8
+//               loads the Q tile, then K_j and V_j, into one ring of 7 to 14
 //               slots (the Q tile takes 2 or 3 slots).
 //   warp 1      MMA issuer + TMEM owner.  S = Q K^T takes Q from TMEM and K
 //               from shared memory, so each S MMA reads only its 64 K rows
@@ -74,11 +74,12 @@ struct TcCfg {
   static constexpr int Q_PER_SLOT = KV_TILE / Q_CHUNK;
   static_assert(Q_PER_SLOT >= 1, "a Q chunk fits a ring slot");
   static constexpr int Q_SLOTS = (KCH + Q_PER_SLOT - 1) / Q_PER_SLOT;
-  // As many ring slots as shared memory holds (at most 8): 7 at d = 256, 8
-  // at d = 192 and d = 96.  A deeper ring starts each load earlier before
-  // its tile is needed.
+  // As many ring slots as shared memory holds (at most 16): 7 at d = dv =
+  // 256, 9 at d = 192, 14 at d = 96.  The loads in flight per SM are bounded
+  // by the ring: a deeper ring starts each load earlier before its tile is
+  // needed, which is what hides the L2 / DRAM latency.
   static constexpr int SLOTS_FIT = (232448 - 64 - 2048) / KV_TILE;
-  static constexpr int SLOTS = SLOTS_FIT < 8 ? SLOTS_FIT : 8;
+  static constexpr int SLOTS = SLOTS_FIT < 16 ? SLOTS_FIT : 16;
   static_assert(SLOTS >= Q_SLOTS + 2, "K/V ring depth");
   static constexpr int OFF_RING = 0;
   static constexpr int OFF_BAR = OFF_RING + SLOTS * KV_TILE;
@@ -104,7 +105,7 @@ struct ItemSlot {
 struct Bars {
   uint64_t q_tmem, o_ready, o_done, o_free, drain;
   uint64_t s_full[2], p_full[2];
-  uint64_t ring_full[8], ring_empty[8];
+  uint64_t ring_full[16], ring_empty[16];
   uint64_t item_full[kItemSlots], item_empty[kItemSlots];
   ItemSlot items[kItemSlots];
 };
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int* next_item = p.ws + WsLayout{p.B, p.Hkv}.counters();
       int idx = atomicAdd(next_item, 1);
       PrefillItem it{};
-      if (idx < h.n_items) it = decode_prefill_item(p, h, idx);
+      if (idx < h.n_items) it = decode_prefill_item(p, h, idx, true);
       while (ok && idx < h.n_items) {
         const int idx_next = idx + 1 < h.n_items ? atomicAdd(next_item, 1) : h.n_items;
         PrefillItem it_next = it;
@@ -319,13 +320,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             c * 64, it.b, g, v.kv_start, k0);
             }
             if (!decoded) {
-              it_next = decode_prefill_item(p, h, idx_next);
+              it_next = decode_prefill_item(p, h, idx_next, true);
               decoded = true;
             }
           }
         }
         if (!ok) break;
-        if (!decoded) it_next = decode_prefill_item(p, h, idx_next);
+        if (!decoded) it_next = decode_prefill_item(p, h, idx_next, true);
         idx = idx_next;
         it = it_next;
       }
