@@ -115,6 +115,21 @@ def test_prefill_extra_head_sizes(d, dv, G):
     check(out, oracle.attention(q, k, v, cq, ck, G * Hkv, Hkv, 0.0, True, 0.0), "bf16")
 
 
+# Single-tile kernel edges: sequences shorter than a query tile, L_kv < L_q
+# (early rows see no key and come out zero), G not dividing 128, and the
+# packed tail shifting the last item's tile back.
+@pytest.mark.parametrize("d,dv", [(192, 128), (96, 96)])
+@pytest.mark.parametrize("G,causal", [(1, True), (3, True), (2, False), (6, True)])
+def test_single_tile_kernel_edges(d, dv, G, causal):
+    Hkv = 2
+    lq = [5, 128, 300, 700, 129, 40, 257]
+    lkv = [5, 100, 300, 900, 1, 700, 257]
+    q, k, v, cq, ck = workloads.make_packed(lq, lkv, G * Hkv, Hkv, d, dv, "bf16",
+                                            seed=7 * d + dv + G)
+    out = run_gpu(q, k, v, cq, ck, G * Hkv, Hkv, 0.0, causal, 0.0)
+    check(out, oracle.attention(q, k, v, cq, ck, G * Hkv, Hkv, 0.0, causal, 0.0), "bf16")
+
+
 # Split-KV decode for every head-size pair of the tensor-core path and every
 # grouping it serves (G = 16 runs as two head groups of 8), with keys enough
 # for several splits and the log-sum-exp combine.
