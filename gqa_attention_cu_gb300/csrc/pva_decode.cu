@@ -15,15 +15,18 @@
 //               publishes each decoded unit through a shared-memory ring, and
 //               streams its K and V tiles of TK keys (16 KB each, rows of d
 //               contiguous elements) into a 4-stage ring.
-//   warps 1..8  compute.  A warp serves GW = min(G, 8) heads; with G = 16
-//               warps 1..4 take heads 0..7 and warps 5..8 heads 8..15 of the
-//               same tiles.  A round covers R = 32/GW keys x GW heads = 32
+//   warps 1..8  compute.  A warp serves GW = min(G, 8) heads (min(G, 4) at
+//               head sizes >= 192); with more heads than that the warps split
+//               into head groups over the same tiles (G = 16, d = 128:
+//               warps 1..4 take heads 0..7 and warps 5..8 heads 8..15).  A round covers R = 32/GW keys x GW heads = 32
 //               (key, head) pairs: lane l owns DPL consecutive dims of every
 //               key (DPL = 2, 4 or 8; lanes past the head size hold zeros), forms
 //               the 32 partial dot products, and a reduce-scatter butterfly
 //               (warp shuffles) leaves the full score of pair l in lane l.
 //               Online softmax per head, probabilities shared through shared
-//               memory, O accumulated per lane over its dims of V.
+//               memory, O accumulated per lane over its dims of V.  Rounds
+//               are dealt to the warps across tiles, so with fewer rounds per
+//               tile than warps (small G) each warp takes whole tiles in turn.
 //   end of unit the 8 warps' (max, sum, O) are merged in a fixed order;
 //               an unsplit unit writes the output row; a split unit writes
 //               its fp32 partial and the last split to finish (device-wide
@@ -48,7 +51,10 @@ __host__ __device__ constexpr int dims_per_lane(int D) { return D <= 64 ? 2 : D 
 
 template <int DK, int DV, int G>
 struct DecCfg {
-  static constexpr int GW = G < 8 ? G : 8;         // heads per warp
+  // Heads per warp: up to 8, or 4 at head sizes >= 192, where the per-lane
+  // q and O of 8 heads (8 dims each) spilled to local memory (d = 256,
+  // G = 8: 2.0 ms -> 1.16 ms for 4.6 GB of K/V).
+  static constexpr int GW = DK >= 192 ? (G < 4 ? G : 4) : (G < 8 ? G : 8);
   static constexpr int HG = G / GW;                // head groups
   static constexpr int NWG = kComputeWarps / HG;   // warps per head group
   static constexpr int TK = decode_tile_keys(DK, DV);  // keys per tile
@@ -332,7 +338,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int base = k0 - un.kv_start;            // local key of tile row 0
         const int lo = un.ks + j * TK - base;          // visible tile rows [lo, hi)
         const int hi = min(un.ks + (j + 1) * TK, un.ke) - base;
-        for (int rd = cwg; rd < C::RPT; rd += C::NWG) {
+        // Rounds are dealt to the head group's warps across tiles: round rd
+        // of tile j goes to warp (j * RPT + rd) mod NWG, so that with fewer
+        // rounds per tile than warps (small G) the warps take whole tiles in
+        // turn instead of leaving most of them idle.
+        const int rd0 = ((cwg - j * C::RPT) % C::NWG + C::NWG) % C::NWG;
+        for (int rd = rd0; rd < C::RPT; rd += C::NWG) {
           const int r0 = rd * R;  // first tile row of this round
           float v[32];
 #pragma unroll
