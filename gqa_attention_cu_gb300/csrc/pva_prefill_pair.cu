@@ -79,7 +79,6 @@ struct ItemSlot {
 struct PairBars {
   uint64_t q_full, q_empty, drain, pad;
   uint64_t s_full[2], p_half[2], p_full[2], o_ready[2], o_free[2];
-  uint64_t pvh_done[2];  // the first half of a tile's P.V MMAs complete
   uint64_t stage_full[2], stage_free[2];  // epilogue staging buffer hand-off
   uint64_t ring_full[kMaxSlots], ring_empty[kMaxSlots];
   uint64_t item_full[kItemSlots], item_empty[kItemSlots];
@@ -121,7 +120,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->p_full[t], 128);
       mbar_init(&bars->o_ready[t], 1);
       mbar_init(&bars->o_free[t], 128);
-      mbar_init(&bars->pvh_done[t], 1);
       mbar_init(&bars->stage_full[t], 128);
       mbar_init(&bars->stage_free[t], 1);
     }
@@ -284,7 +282,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = k0; kk < k1; ++kk)
           mma_ts(tmem + C::COL_O + t * D, tmem + C::COL_S + t * 128 + kk * 8,
                  sdesc_advance(va, kk * 16 * 128), idesc_o, (!first || kk > 0) ? 1u : 0u);
-        if (k1 == BN / 32) mma_commit(&bars->pvh_done[t]);
         if (k1 == BN / 16) mma_commit(&bars->o_ready[t]);
       }
     };
@@ -420,86 +417,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                              ? kHalfEmpty
                          : __all_sync(0xffffffffu, lo_c <= c) ? kMaskHi
                                                                : kMaskBoth;
-        }
-        // From an item's second key tile on, every row of the warp has a
-        // finite running maximum m_used.  The two-pass path below reads S once
-        // for the tile's maximum and again for the exponentials, which are
-        // taken against the stale m_used unless the maximum grows by more
-        // than the rescale threshold.  The one-pass path reads each half of S
-        // once, exponentiates it against m_used while tracking its largest
-        // exponent, and only when that exceeds the threshold (rare) rescales
-        // O and redoes the half against the grown maximum: the same values
-        // without the separate pass for the maximum.
-        const bool one_pass = !__any_sync(0xffffffffu, m_used == NEG_INF);
-        if (one_pass) {
-#pragma unroll
-          for (int c = 0; c < BN; c += 64) {
-            const int md = mode[c / 64];
-            uint32_t pw[32];
-            float2 rs = make_float2(0.0f, 0.0f);
-            if (md == kHalfEmpty) {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) pw[e] = 0u;
-            } else {
-              uint32_t va[32], vb[32];
-              tmem_ld32(t_lane + col_s + c, va);
-              tmem_ld32(t_lane + col_s + c + 32, vb);
-              tmem_wait_ld();
-              float xm;
-              if (md == kMaskNone)
-                exp64<T, CAP, kMaskNone, true>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_used, rs,
-                                               pw, &xm);
-              else if (md == kMaskHi)
-                exp64<T, CAP, kMaskHi, true>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_used, rs,
-                                             pw, &xm);
-              else
-                exp64<T, CAP, kMaskBoth, true>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_used, rs,
-                                               pw, &xm);
-              if (__any_sync(0xffffffffu, xm > kRescaleThreshold)) {
-                const float grow = xm > kRescaleThreshold ? xm : 0.0f;
-                const float a = ex2_approx(-grow);
-                // O must hold every P.V of the item issued so far: those of
-                // the tiles before j (see the two-pass path) and, for the
-                // second half, the first half's of this tile.
-                if (c > 0) {
-                  ok = __all_sync(0xffffffffu,
-                                  mbar_wait<false>(&bars->pvh_done[tq], T_ & 1, abort, status));
-                  if (!ok) break;
-                  tc_fence_after();
-                }
-#pragma unroll 1
-                for (int cc = 0; cc < D; cc += 32) {
-                  uint32_t v[32];
-                  tmem_ld32(t_lane + col_o + cc, v);
-                  tmem_wait_ld();
-#pragma unroll
-                  for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
-                  tmem_st32(t_lane + col_o + cc, v);
-                }
-                l *= a;
-                m_used += grow;
-                // this half of S is still in TMEM (its P is written below)
-                tmem_ld32(t_lane + col_s + c, va);
-                tmem_ld32(t_lane + col_s + c + 32, vb);
-                tmem_wait_ld();
-                tmem_wait_st();
-                rs = make_float2(0.0f, 0.0f);
-                if (md == kMaskNone)
-                  exp64<T, CAP, kMaskNone>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_used, rs, pw);
-                else if (md == kMaskHi)
-                  exp64<T, CAP, kMaskHi>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_used, rs, pw);
-                else
-                  exp64<T, CAP, kMaskBoth>(va, vb, c, lo_c, hi_c, s_mul, cap_mul, m_used, rs, pw);
-              }
-            }
-            tmem_st32(t_lane + col_s + (c >> 1), pw);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(c == 0 ? &bars->p_half[tq] : &bars->p_full[tq]);
-            l += rs.x + rs.y;
-          }
-          if (!ok) break;
-          continue;
         }
         // Pass 1: extreme raw score over the visible columns.  The score
         // transform (scale, then optional softcap) is monotone -- increasing

@@ -55,19 +55,14 @@ __device__ __forceinline__ float extreme64(const uint32_t (&va)[32], const uint3
 // sweeps -- all exponents, then all ex2, then sums and packing -- so that 16
 // independent ex2 are issued back to back rather than each waiting for the
 // one before it.
-//
-// TRACK: also returns in *xmax the largest exponent x - m of the visible
-// columns (-inf when none is visible), for a caller that exponentiates
-// against a running maximum before knowing this tile's own maximum.
-template <typename T, bool CAP, int MASK, bool TRACK = false>
+template <typename T, bool CAP, int MASK>
 __device__ __forceinline__ void exp64(const uint32_t (&va)[32], const uint32_t (&vb)[32], int c,
                                       int lo_c, int hi_c, float s_mul, float cap_mul, float m_eff,
-                                      float2& rs, uint32_t (&pw)[32], float* xmax = nullptr) {
+                                      float2& rs, uint32_t (&pw)[32]) {
   const float2 mul2 = make_float2(s_mul, s_mul), neg_m = make_float2(-m_eff, -m_eff);
   const unsigned span = hi_c > lo_c ? (unsigned)(hi_c - lo_c) : 0u;
   const float ninf = __int_as_float(0xff800000);
   float2 acc[2] = {rs, make_float2(0.0f, 0.0f)};  // two independent partial sums
-  float xm[2] = {ninf, ninf};                      // two independent partial maxima
 #pragma unroll
   for (int g = 0; g < 32; g += 8) {
     float2 x[8];
@@ -85,7 +80,6 @@ __device__ __forceinline__ void exp64(const uint32_t (&va)[32], const uint32_t (
         x[k].x = col_visible<MASK>(c + e, lo_c, hi_c, span) ? x[k].x : ninf;
         x[k].y = col_visible<MASK>(c + e + 1, lo_c, hi_c, span) ? x[k].y : ninf;
       }
-      if (TRACK) xm[k & 1] = fmax3f(xm[k & 1], x[k].x, x[k].y);
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) x[k] = make_float2(ex2_approx(x[k].x), ex2_approx(x[k].y));
@@ -96,7 +90,6 @@ __device__ __forceinline__ void exp64(const uint32_t (&va)[32], const uint32_t (
     }
   }
   rs = fadd2(acc[0], acc[1]);
-  if (TRACK) *xmax = fmaxf(xm[0], xm[1]);
 }
 
 }  // namespace pva
