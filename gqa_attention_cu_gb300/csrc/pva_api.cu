@@ -213,13 +213,14 @@ int check_and_plan(const void* q, const void* k, const void* v, const int32_t* c
     // The split-KV decode kernel covers every head-size pair of the
     // tensor-core path with G in {1, 2, 4, 8, 16}; other groupings take their
     // single-row sequences through the prefill kernel.  For d == dv in
-    // {64, 128, 256} with G <= 8 it reads K/V at close to copy bandwidth and
-    // takes every single-row sequence; for the other shapes (G = 16, head
-    // sizes 96 and 192) it is limited by its arithmetic, and the scheduler
-    // gives it single-row sequences only when they are too few to keep every
-    // SM busy in the prefill kernel (which does not split keys).
+    // {64, 128} with G <= 4 and d == dv == 256 with G <= 2 it reads K/V at
+    // close to copy bandwidth and takes every single-row sequence; for the
+    // other shapes (G = 8 and 16, d = 256 with G = 4, head sizes 96 and 192)
+    // its arithmetic per K/V byte limits it, and the scheduler gives it
+    // single-row sequences only when they are too few to keep every SM busy
+    // in the prefill kernel (which does not split keys).
     plan->decode = G == 1 || G == 2 || G == 4 || G == 8 || G == 16;
-    const bool tuned = G <= 8 && d == dv && (d == 64 || d == 128 || d == 256);
+    const bool tuned = d == dv && (((d == 64 || d == 128) && G <= 4) || (d == 256 && G <= 2));
     plan->sched = SchedConfig{(kTcRows / G) * tc_tiles_per_item(d, dv), Hkv, tc_block_n(d, dv),
                               plan->decode ? 1 : 0, 0, plan->decode && !tuned ? 1 : 0};
   }

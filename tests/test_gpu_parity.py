@@ -422,7 +422,7 @@ def sched_mirror(lq, lkv, H, Hkv, d, dtype, num_sms, dv=None):
         paired = d == dv and d in (64, 128)
         tile, units = (128 // G) * (2 if paired else 1), Hkv
         dec = G in (1, 2, 4, 8, 16)
-        tuned = G <= 8 and d == dv and d in (64, 128, 256)
+        tuned = d == dv and ((d in (64, 128) and G <= 4) or (d == 256 and G <= 2))
         if dec and not tuned:  # adaptive: only when too few to fill the SMs
             dec = sum(1 for a in lq if a == 1) * Hkv < 2 * num_sms
     cap = min(B * Hkv * 16, 16384)
