@@ -60,6 +60,9 @@ def load_library(path: str | None = None):
         lib.pva_forward.restype = i
         lib.pva_forward_local.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, f, i, i,
                                           vp]
+        lib.pva_forward_from_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i,
+                                              i, i, f, i, f, i, i, vp]
+        lib.pva_forward_from_host.restype = i
         lib.pva_forward_local.restype = i
         lib.pva_forward_padded.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, f, i,
                                            vp]
@@ -129,6 +132,28 @@ def pva_forward(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, B: int, num_heads: in
                          cu_seqlens_kv.data_ptr(), out.data_ptr(), int(B), int(num_heads),
                          int(kv_num_heads), int(head_size), int(v_head_size), float(scale),
                          int(is_causal), float(softcap), code, _stream_ptr(stream))
+    _check(rc)
+
+
+def pva_forward_from_host(q_host, k_host, v_host, cu_seqlens_q_host, cu_seqlens_kv_host,
+                          out_host, q_dev, k_dev, v_dev, out_dev, cu_dev, B: int,
+                          num_heads: int, kv_num_heads: int, head_size: int, v_head_size: int,
+                          scale: float = 0.0, is_causal: int = 0, softcap: float = 0.0,
+                          chunks: int = 0, dtype: int | None = None, stream=None) -> None:
+    """pva_forward on a batch in host memory (the *_host tensors, pinned for
+    overlap; the offsets are host int32 tensors): the call copies it into the
+    caller's device buffers (*_dev, cu_dev of >= 4 B + 34 int32) chunk by
+    chunk, overlapping the copies with the attention, and copies the output
+    back into out_host; ``stream`` completes after the last copy."""
+    lib = load_library()
+    code = _dtype_code(q_host) if dtype is None else int(dtype)
+    rc = lib.pva_forward_from_host(q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(),
+                                   cu_seqlens_q_host.data_ptr(), cu_seqlens_kv_host.data_ptr(),
+                                   out_host.data_ptr(), q_dev.data_ptr(), k_dev.data_ptr(),
+                                   v_dev.data_ptr(), out_dev.data_ptr(), cu_dev.data_ptr(),
+                                   int(B), int(num_heads), int(kv_num_heads), int(head_size),
+                                   int(v_head_size), float(scale), int(is_causal),
+                                   float(softcap), code, int(chunks), _stream_ptr(stream))
     _check(rc)
 
 

@@ -489,6 +489,64 @@ int forward_impl(const Spec& s, void* stream_) {
   return PVA_OK;
 }
 
+// ---- host-buffer entry point (pva_forward_from_host) -------------------------
+constexpr int kMaxChunks = 16;
+
+struct ChunkBounds {
+  int n;                   // chunks
+  int b0[kMaxChunks + 1];  // first sequence of each chunk; b0[n] = B
+};
+
+// Offsets of each chunk rebased to its first sequence: chunk c's sequences
+// [b0[c], b0[c+1]) get cu - cu[b0[c]], written from index b0[c] + c on (one
+// block per chunk).
+__global__ void pva_rebase_kernel(const int32_t* cu_q, const int32_t* cu_kv, ChunkBounds cb,
+                                  int32_t* out_q, int32_t* out_kv) {
+  const int c = blockIdx.x;
+  if (c >= cb.n) return;
+  const int b0 = cb.b0[c], b1 = cb.b0[c + 1];
+  const int q0 = cu_q[b0], k0 = cu_kv[b0];
+  for (int i = threadIdx.x; i <= b1 - b0; i += blockDim.x) {
+    out_q[b0 + c + i] = cu_q[b0 + i] - q0;
+    out_kv[b0 + c + i] = cu_kv[b0 + i] - k0;
+  }
+}
+
+// Copy streams and events of the host-buffer entry point, one set per device.
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t in_ev[kMaxChunks] = {}, comp_ev[kMaxChunks] = {};
+};
+std::mutex g_pipe_mu;
+std::map<int, HostPipe> g_pipe;
+
+int get_pipe(int dev, HostPipe** out) {
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.ready) {
+    cudaError_t e;
+    if (!hp.in && (e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking)) != cudaSuccess)
+      return cuda_fail(e, "cudaStreamCreateWithFlags");
+    if (!hp.out && (e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking)) != cudaSuccess)
+      return cuda_fail(e, "cudaStreamCreateWithFlags");
+    cudaEvent_t* evs[2 + 2 * kMaxChunks];
+    int ne = 0;
+    evs[ne++] = &hp.start;
+    evs[ne++] = &hp.done;
+    for (int c = 0; c < kMaxChunks; ++c) {
+      evs[ne++] = &hp.in_ev[c];
+      evs[ne++] = &hp.comp_ev[c];
+    }
+    for (int i = 0; i < ne; ++i)
+      if (!*evs[i] && (e = cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventCreateWithFlags");
+    hp.ready = true;
+  }
+  *out = &hp;
+  return PVA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -714,6 +772,119 @@ void pva_release(void) {
       ++it;
     }
   }
+}
+
+int pva_forward_from_host(const void* q_host, const void* k_host, const void* v_host,
+                          const int32_t* cu_seqlens_q_host, const int32_t* cu_seqlens_kv_host,
+                          void* out_host, void* q_dev, void* k_dev, void* v_dev, void* out_dev,
+                          int32_t* cu_dev, int B, int num_heads, int kv_num_heads, int head_size,
+                          int v_head_size, float scale, int is_causal, float softcap, int dtype,
+                          int chunks, void* stream_) {
+  if (B < 1 || !cu_seqlens_q_host || !cu_seqlens_kv_host || !cu_dev)
+    return fail(PVA_ERR_INVALID_ARG, "B >= 1 and the offset arrays are required");
+  if (num_heads <= 0 || kv_num_heads <= 0 || head_size <= 0 || v_head_size <= 0)
+    return fail(PVA_ERR_INVALID_ARG, "head counts and sizes must be positive");
+  if (dtype != PVA_F32 && dtype != PVA_F16 && dtype != PVA_BF16)
+    return fail(PVA_ERR_INVALID_ARG, "dtype must be PVA_F32, PVA_F16 or PVA_BF16");
+  // The copies are sized from the offsets, so they are checked here, on the
+  // host, before anything is enqueued.
+  if (cu_seqlens_q_host[0] != 0 || cu_seqlens_kv_host[0] != 0)
+    return fail(PVA_ERR_INVALID_ARG, "cu_seqlens must start at 0");
+  for (int b = 0; b < B; ++b)
+    if (cu_seqlens_q_host[b + 1] < cu_seqlens_q_host[b] ||
+        cu_seqlens_kv_host[b + 1] < cu_seqlens_kv_host[b])
+      return fail(PVA_ERR_INVALID_ARG, "cu_seqlens must be non-decreasing");
+  const long long tq = cu_seqlens_q_host[B], tk = cu_seqlens_kv_host[B];
+  if ((tq > 0 && (!q_host || !q_dev || !out_host || !out_dev)) ||
+      (tk > 0 && (!k_host || !v_host || !k_dev || !v_dev)))
+    return fail(PVA_ERR_INVALID_ARG, "null buffer with a non-empty extent");
+  const size_t esz = dtype == PVA_F32 ? 4 : 2;
+  const size_t rq = (size_t)num_heads * head_size * esz, ro = (size_t)num_heads * v_head_size * esz;
+  const size_t rk = (size_t)kv_num_heads * head_size * esz;
+  const size_t rv = (size_t)kv_num_heads * v_head_size * esz;
+  // Chunks: runs of whole sequences moving about equal bytes.
+  int n = chunks <= 0 ? 8 : chunks;
+  n = n < kMaxChunks ? n : kMaxChunks;
+  n = n < B ? n : B;
+  ChunkBounds cb{};
+  {
+    const double total = (double)tq * (rq + ro) + (double)tk * (rk + rv);
+    double acc = 0.0;
+    int c = 0;
+    for (int b = 0; b + 1 < B && c + 1 < n; ++b) {
+      acc += (double)(cu_seqlens_q_host[b + 1] - cu_seqlens_q_host[b]) * (rq + ro) +
+             (double)(cu_seqlens_kv_host[b + 1] - cu_seqlens_kv_host[b]) * (rk + rv);
+      if (acc >= total * (c + 1) / n) cb.b0[++c] = b + 1;
+    }
+    cb.n = c + 1;
+    cb.b0[cb.n] = B;
+  }
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  cudaStream_t s = static_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  HostPipe* hp = nullptr;
+  int rc = get_pipe(dev, &hp);
+  if (rc != PVA_OK) return rc;
+  auto ck = [&](cudaError_t err, const char* what) { return err == cudaSuccess ? PVA_OK : cuda_fail(err, what); };
+  // The copies start after the work already on `stream`, which may still read
+  // the device buffers.
+  if ((rc = ck(cudaEventRecord(hp->start, s), "cudaEventRecord")) != PVA_OK ||
+      (rc = ck(cudaStreamWaitEvent(hp->in, hp->start, 0), "cudaStreamWaitEvent")) != PVA_OK)
+    return rc;
+  int32_t* cu_q_d = cu_dev;
+  int32_t* cu_kv_d = cu_dev + (B + 1);
+  int32_t* rq_d = cu_dev + 2 * (B + 1);
+  int32_t* rkv_d = rq_d + (B + kMaxChunks);
+  if ((rc = ck(cudaMemcpyAsync(cu_q_d, cu_seqlens_q_host, (B + 1) * sizeof(int32_t),
+                               cudaMemcpyHostToDevice, hp->in), "cudaMemcpyAsync")) != PVA_OK ||
+      (rc = ck(cudaMemcpyAsync(cu_kv_d, cu_seqlens_kv_host, (B + 1) * sizeof(int32_t),
+                               cudaMemcpyHostToDevice, hp->in), "cudaMemcpyAsync")) != PVA_OK)
+    return rc;
+  pva_rebase_kernel<<<cb.n, 128, 0, hp->in>>>(cu_q_d, cu_kv_d, cb, rq_d, rkv_d);
+  if ((rc = ck(cudaGetLastError(), "pva_rebase_kernel launch")) != PVA_OK) return rc;
+  auto at = [](const void* base, size_t off) {
+    return const_cast<char*>(static_cast<const char*>(base)) + off;
+  };
+  for (int c = 0; c < cb.n; ++c) {
+    const int b0 = cb.b0[c], b1 = cb.b0[c + 1];
+    const size_t q0 = cu_seqlens_q_host[b0], q1 = cu_seqlens_q_host[b1];
+    const size_t k0 = cu_seqlens_kv_host[b0], k1 = cu_seqlens_kv_host[b1];
+    // this chunk's rows in, on the copy-in stream
+    if (q1 > q0 && (rc = ck(cudaMemcpyAsync(at(q_dev, q0 * rq), at(q_host, q0 * rq), (q1 - q0) * rq,
+                                            cudaMemcpyHostToDevice, hp->in), "cudaMemcpyAsync")) != PVA_OK)
+      return rc;
+    if (k1 > k0 &&
+        ((rc = ck(cudaMemcpyAsync(at(k_dev, k0 * rk), at(k_host, k0 * rk), (k1 - k0) * rk,
+                                  cudaMemcpyHostToDevice, hp->in), "cudaMemcpyAsync")) != PVA_OK ||
+         (rc = ck(cudaMemcpyAsync(at(v_dev, k0 * rv), at(v_host, k0 * rv), (k1 - k0) * rv,
+                                  cudaMemcpyHostToDevice, hp->in), "cudaMemcpyAsync")) != PVA_OK))
+      return rc;
+    if ((rc = ck(cudaEventRecord(hp->in_ev[c], hp->in), "cudaEventRecord")) != PVA_OK ||
+        (rc = ck(cudaStreamWaitEvent(s, hp->in_ev[c], 0), "cudaStreamWaitEvent")) != PVA_OK)
+      return rc;
+    // its attention on `stream`
+    if (q1 > q0 &&
+        (rc = pva_forward(at(q_dev, q0 * rq), k1 > k0 ? at(k_dev, k0 * rk) : k_dev,
+                          k1 > k0 ? at(v_dev, k0 * rv) : v_dev, rq_d + b0 + c, rkv_d + b0 + c,
+                          at(out_dev, q0 * ro), b1 - b0, num_heads, kv_num_heads, head_size,
+                          v_head_size, scale, is_causal, softcap, dtype, s)) != PVA_OK)
+      return rc;
+    // and its output rows back, on the copy-out stream
+    if ((rc = ck(cudaEventRecord(hp->comp_ev[c], s), "cudaEventRecord")) != PVA_OK ||
+        (rc = ck(cudaStreamWaitEvent(hp->out, hp->comp_ev[c], 0), "cudaStreamWaitEvent")) != PVA_OK)
+      return rc;
+    if (q1 > q0 && (rc = ck(cudaMemcpyAsync(at(out_host, q0 * ro), at(out_dev, q0 * ro),
+                                            (q1 - q0) * ro, cudaMemcpyDeviceToHost, hp->out),
+                            "cudaMemcpyAsync")) != PVA_OK)
+      return rc;
+  }
+  // `stream` completes after the last output copy.
+  if ((rc = ck(cudaEventRecord(hp->done, hp->out), "cudaEventRecord")) != PVA_OK ||
+      (rc = ck(cudaStreamWaitEvent(s, hp->done, 0), "cudaStreamWaitEvent")) != PVA_OK)
+    return rc;
+  return PVA_OK;
 }
 
 int pva_version(void) { return (0 << 16) | (1 << 8) | 0; }

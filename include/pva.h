@@ -108,6 +108,41 @@ int pva_forward(const void* q, const void* k, const void* v,
                 float softcap, int dtype, void* stream);
 
 /*
+ * pva_forward_from_host -- pva_forward for a batch held in host memory: the
+ * same attention (packed_varlen_attention.rs, stages 1-5), with the copies in
+ * and out of the device done by the call and overlapped with the attention.
+ *
+ * q_host, k_host, v_host, out_host : host buffers in the packed layouts of
+ *                pva_forward (pinned memory lets the copies overlap the
+ *                attention; pageable memory works but copies synchronously).
+ * cu_seqlens_q_host, cu_seqlens_kv_host : HOST int32 [B+1] offsets, read by
+ *                the call (starting at 0, non-decreasing; else
+ *                PVA_ERR_INVALID_ARG with nothing enqueued).
+ * q_dev, k_dev, v_dev, out_dev : device buffers of the same sizes as the host
+ *                ones, owned by the caller; the call overwrites them.
+ * cu_dev       : device int32 scratch of at least 4 * B + 34 words.
+ * chunks       : runs of whole sequences moved and computed in turn (0: 8;
+ *                at most 16 and at most B), cut to move about equal bytes:
+ *                chunk c+1 is copied in while chunk c is computed and chunk
+ *                c-1 copied out, on two library streams synchronised with
+ *                `stream` by events.  Each chunk is one pva_forward call on
+ *                `stream` (with offsets rebased on the device), so every row
+ *                offset must keep pva_forward's 16-byte alignment.
+ * Other arguments: as pva_forward.
+ *
+ * Returns PVA_OK once all work is enqueued; `stream` completes after the last
+ * output copy.  The copies start after the work already on `stream`.  An
+ * error from a chunk's pva_forward is returned as it is (earlier chunks'
+ * work stays enqueued).  Calls on one device are serialised by a lock.
+ */
+int pva_forward_from_host(const void* q_host, const void* k_host, const void* v_host,
+                          const int32_t* cu_seqlens_q_host, const int32_t* cu_seqlens_kv_host,
+                          void* out_host, void* q_dev, void* k_dev, void* v_dev, void* out_dev,
+                          int32_t* cu_dev, int B, int num_heads, int kv_num_heads, int head_size,
+                          int v_head_size, float scale, int is_causal, float softcap, int dtype,
+                          int chunks, void* stream);
+
+/*
  * pva_forward_local -- pva_forward with a local (sliding) attention window,
  * the `local_window` of the softmax and grouped-query reference kernels on the
  * attention.rs and group_query_attention.rs pages.  With local_window = W > 0,

@@ -131,3 +131,35 @@ def test_kvcache_host_argument_checks_need_no_gpu(lib, kw, code):
     dimensions and tables, rotary with k_seq not in {0, q_seq}, table types."""
     assert _call_kvcache(lib, **kw) == code
     assert pva.pva_last_error() != ""
+
+
+def _call_from_host(lib, cq, ck, **kw):
+    import ctypes
+    B = len(cq) - 1
+    cq_a = (ctypes.c_int32 * len(cq))(*cq)
+    ck_a = (ctypes.c_int32 * len(ck))(*ck)
+    args = dict(buf=16, cu=16, B=B, H=4, Hkv=2, d=128, dv=128, dtype=2, chunks=0)
+    args.update(kw)
+    b = args["buf"]
+    return lib.pva_forward_from_host(b, b, b, ctypes.addressof(cq_a), ctypes.addressof(ck_a), b,
+                                     b, b, b, b, args["cu"], args["B"], args["H"], args["Hkv"],
+                                     args["d"], args["dv"], 0.0, 1, 0.0, args["dtype"],
+                                     args["chunks"], None)
+
+
+@pytest.mark.parametrize("cq,ck,kw", [
+    ([1, 3], [0, 3], {}),                 # offsets not starting at 0
+    ([0, 3], [1, 3], {}),
+    ([0, 3, 2], [0, 3, 4], {}),           # decreasing
+    ([0, 3, 4], [0, 5, 4], {}),
+    ([0, 3], [0, 3], dict(B=0)),
+    ([0, 3], [0, 3], dict(cu=None)),
+    ([0, 3], [0, 3], dict(buf=None)),     # null buffers with rows to move
+    ([0, 3], [0, 3], dict(H=0)),
+    ([0, 3], [0, 3], dict(dtype=5)),
+])
+def test_forward_from_host_checks_offsets_on_the_host(lib, cq, ck, kw):
+    """pva_forward_from_host sizes its copies from the host offsets, so it
+    rejects malformed ones (and missing buffers) before any CUDA call."""
+    assert _call_from_host(lib, cq, ck, **kw) == -1
+    assert pva.pva_last_error() != ""

@@ -98,3 +98,17 @@ def test_errors_raise_with_the_library_text(monkeypatch):
     with pytest.raises(pva.PvaError, match="B must be >= 1"):
         pva.pva_forward(_t(1, 1, 64), _t(1, 1, 64), _t(1, 1, 64), _t(1, dtype=torch.int32),
                         _t(1, dtype=torch.int32), _t(1, 1, 64), 0, 1, 1, 64, 64, stream=0)
+
+
+def test_forward_from_host_marshalling(rec):
+    qh, kh, vh, oh = _t(10, 8, 64), _t(12, 2, 64), _t(12, 2, 48), _t(10, 8, 48)
+    qd, kd, vd, od = _t(10, 8, 64), _t(12, 2, 64), _t(12, 2, 48), _t(10, 8, 48)
+    cq, ck = _t(3, dtype=torch.int32), _t(3, dtype=torch.int32)
+    cu = _t(4 * 2 + 34, dtype=torch.int32)
+    pva.pva_forward_from_host(qh, kh, vh, cq, ck, oh, qd, kd, vd, od, cu, 2, 8, 2, 64, 48,
+                              0.25, 1, 30.0, chunks=3, stream=5)
+    name, a = rec.calls[-1]
+    assert name == "pva_forward_from_host"
+    assert a == (qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), cq.data_ptr(), ck.data_ptr(),
+                 oh.data_ptr(), qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(),
+                 cu.data_ptr(), 2, 8, 2, 64, 48, 0.25, 1, 30.0, 2, 3, 5)
