@@ -758,11 +758,26 @@ const char* pva_status_string(int code) {
 const char* pva_last_error(void) { return g_last_error.c_str(); }
 
 void pva_release(void) {
+  std::lock_guard<std::mutex> pipe_lock(g_pipe_mu);
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return;
   cudaDeviceSynchronize();
   noalloc_forget_device(dev);
+  auto hp = g_pipe.find(dev);
+  if (hp != g_pipe.end()) {
+    HostPipe& h = hp->second;
+    if (h.in) cudaStreamDestroy(h.in);
+    if (h.out) cudaStreamDestroy(h.out);
+    cudaEvent_t evs[2 + 2 * kMaxChunks] = {h.start, h.done};
+    for (int c = 0; c < kMaxChunks; ++c) {
+      evs[2 + 2 * c] = h.in_ev[c];
+      evs[3 + 2 * c] = h.comp_ev[c];
+    }
+    for (cudaEvent_t e : evs)
+      if (e) cudaEventDestroy(e);
+    g_pipe.erase(hp);
+  }
   for (auto it = g_ws.begin(); it != g_ws.end();) {
     if (it->first.first == dev) {
       if (it->second.buf) cudaFree(it->second.buf);

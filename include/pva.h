@@ -347,7 +347,8 @@ const char* pva_status_string(int code);
 const char* pva_last_error(void);
 
 /* Frees every workspace the library holds on the current device (waits for
- * the streams that used them first), and drops pva_forward_noalloc's cached
+ * the streams that used them first), destroys the copy streams and events of
+ * pva_forward_from_host there, and drops pva_forward_noalloc's cached
  * address of its static scratch on that device. */
 void pva_release(void);
 

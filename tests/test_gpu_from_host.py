@@ -74,3 +74,14 @@ def test_fp32_batch_and_empty_chunks():
     q, k, v, cq, ck = workloads.make_packed(lq, lkv, 4, 4, 64, 64, "f32", seed=53)
     got = _host_call(q, k, v, cq, ck, 4, 4, 64, 64, False, 0.0, 7)
     check(got, oracle.attention(q, k, v, cq, ck, 4, 4, 0.0, False, 0.0), "f32")
+
+
+def test_release_between_calls():
+    """pva_release destroys the entry point's copy streams and events; the
+    next call creates them again."""
+    lq, lkv = [40, 1, 300], [40, 700, 300]
+    q, k, v, cq, ck = workloads.make_packed(lq, lkv, 8, 2, 128, 128, "bf16", seed=54)
+    ref = oracle.attention(q, k, v, cq, ck, 8, 2, 0.0, True, 0.0)
+    check(_host_call(q, k, v, cq, ck, 8, 2, 128, 128, True, 0.0, 2), ref, "bf16")
+    pva.pva_release()
+    check(_host_call(q, k, v, cq, ck, 8, 2, 128, 128, True, 0.0, 2), ref, "bf16")
