@@ -286,6 +286,20 @@ def test_running_maximum_growing_across_and_within_key_tiles(d, causal):
     check(out, oracle.attention(q, k, v, cq, ck, 8, 2, 0.0, causal, 0.0), "bf16")
 
 
+# A negative scale flips the direction of the score transform: every kernel
+# takes the row's extreme from the other side (the paired kernel by template,
+# the single-tile kernel's one-pass and two-pass paths by the sign, the
+# decode kernel through its running maximum).  Prefill and single-row
+# sequences, with and without a softcap.
+@pytest.mark.parametrize("d,dv", [(128, 128), (64, 64), (256, 256), (192, 128)])
+@pytest.mark.parametrize("softcap", [0.0, 20.0])
+def test_negative_scale_every_kernel(d, dv, softcap):
+    lq, lkv = [200, 1, 77, 1, 300], [260, 900, 77, 40, 300]
+    q, k, v, cq, ck = workloads.make_packed(lq, lkv, 8, 2, d, dv, "bf16", seed=9 * d + dv)
+    out = run_gpu(q, k, v, cq, ck, 8, 2, -0.07, True, softcap)
+    check(out, oracle.attention(q, k, v, cq, ck, 8, 2, -0.07, True, softcap), "bf16")
+
+
 def test_explicit_scale():
     parity([64, 10], [64, 90], 4, 4, 64, "bf16", causal=False, scale=0.05, seed=27)
 
@@ -603,3 +617,7 @@ def test_bounded_wait_gives_up_with_status_and_context_survives():
     parity([33, 5], [40, 5], 8, 2, 128, "bf16", causal=True, seed=41)
     assert pva.pva_get_status() == 0
     del t0
+
+
+def test_negative_scale_fp32():
+    parity([33, 1, 70], [40, 90, 70], 4, 2, 64, "f32", causal=True, scale=-0.2, seed=57)
