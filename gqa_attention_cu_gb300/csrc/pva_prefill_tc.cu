@@ -40,11 +40,10 @@
 // tile has |t| <= 1/4; otherwise from the identity
 // tanh(t) = 1 - 2 / (exp(2t) + 1).
 //
-// Key tiles that no row of a warp masks, after the rows' first visible tile,
-// are exponentiated in one pass against the running maximum; the pass also
-// finds the largest exponent (and series argument), and the rare tile that
-// would need a larger maximum (or leaves the series range) is redone with
-// the maximum taken first.
+// Softmax per tile in two passes: the row extreme of the raw scores (the
+// score transform is monotone), then the exponentials against the running
+// maximum, which is raised (and O rescaled) only when it grows by more than
+// 2^8.
 #include "pva_device.cuh"
 #include "pva_items.cuh"
 
@@ -140,21 +139,17 @@ __device__ __forceinline__ void extremes64(const uint32_t (&va)[32], const uint3
 // u - u^3/3 + 2u^5/15, with A folded into the coefficients (u * (A + w *
 // (-A/3 + w * 2A/15)), w = u^2); the series alternates with falling terms,
 // so the error is below the next one, 17/315 |u|^7 < 3.3e-6.  MODE 2: tanh
-// from exp/rcp.  TRACK also returns the largest x - m and (MODE 1) the
-// largest w, with which a caller checks a guessed m and the series range
-// after the fact.
-template <typename T, int MODE, bool MASKED, bool TRACK = false>
+// from exp/rcp.
+template <typename T, int MODE, bool MASKED>
 __device__ __forceinline__ float exp64(const uint32_t (&va)[32], const uint32_t (&vb)[32],
                                        int lo_c, int hi_c, float s_mul, float cap_mul,
-                                       float m_eff, uint32_t (&pw)[32], float* xmax = nullptr,
-                                       float* wmax = nullptr) {
+                                       float m_eff, uint32_t (&pw)[32]) {
   const float2 z = make_float2(0.0f, 0.0f);
   const float2 mul2 = make_float2(s_mul, s_mul), neg_m = make_float2(-m_eff, -m_eff);
   const float2 a2 = make_float2(cap_mul, cap_mul);
   const float2 c1 = make_float2(cap_mul * (-1.0f / 3.0f), cap_mul * (-1.0f / 3.0f));
   const float2 c2 = make_float2(cap_mul * (2.0f / 15.0f), cap_mul * (2.0f / 15.0f));
   float2 acc[2] = {z, z};
-  float xm[2] = {__int_as_float(0xff800000), __int_as_float(0xff800000)}, wm[2] = {0.0f, 0.0f};
 #pragma unroll
   for (int e = 0; e < 64; e += 2) {
     const float2 s = make_float2(col32(va, vb, e), col32(va, vb, e + 1));
@@ -165,7 +160,6 @@ __device__ __forceinline__ float exp64(const uint32_t (&va)[32], const uint32_t 
       const float2 u = ffma2(s, mul2, z);
       const float2 w = ffma2(u, u, z);
       x = ffma2(u, ffma2(w, ffma2(w, c2, c1), a2), neg_m);
-      if (TRACK) wm[(e >> 1) & 1] = fmax3f(wm[(e >> 1) & 1], w.x, w.y);
     } else {
       x.x = fmaf(cap_mul, tanh_via_exp2(s.x * s_mul), -m_eff);
       x.y = fmaf(cap_mul, tanh_via_exp2(s.y * s_mul), -m_eff);
@@ -175,14 +169,9 @@ __device__ __forceinline__ float exp64(const uint32_t (&va)[32], const uint32_t 
       x.x = (e >= lo_c && e < hi_c) ? x.x : ninf;
       x.y = (e + 1 >= lo_c && e + 1 < hi_c) ? x.y : ninf;
     }
-    if (TRACK) xm[(e >> 1) & 1] = fmax3f(xm[(e >> 1) & 1], x.x, x.y);
     const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
     acc[(e >> 1) & 1] = fadd2(acc[(e >> 1) & 1], p);
     pw[e >> 1] = pack2<T>(p.x, p.y);
-  }
-  if (TRACK) {
-    *xmax = fmaxf(xm[0], xm[1]);
-    if (MODE == 1) *wmax = fmaxf(wm[0], wm[1]);
   }
   const float2 r = fadd2(acc[0], acc[1]);
   return r.x + r.y;
@@ -547,23 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool masked = !__all_sync(0xffffffffu, lo_c <= 0 && hi_c >= BN);
         uint32_t pw[32];
         float rs, alpha = 1.0f;
-        // An unmasked tile after the row's first visible one is exponentiated
-        // once against the running maximum m, tracking the largest exponent
-        // (and, with a softcap, the series argument): the maximum only has
-        // to be raised when an exponent exceeds the rescale threshold, which
-        // after the first tiles is rare.  Then, or when the series range is
-        // left, the tile is redone as below.
-        bool redo = masked || !__all_sync(0xffffffffu, m_used != NEG_INF);
-        if (!redo) {
-          float xm, wm = 0.0f;
-          if (!CAP)
-            rs = exp64<T, 0, false, true>(va, vb, 0, BN, s_mul, cap_mul, m_used, pw, &xm);
-          else
-            rs = exp64<T, 1, false, true>(va, vb, 0, BN, s_mul, cap_mul, m_used, pw, &xm, &wm);
-          redo = __any_sync(0xffffffffu,
-                            xm > kRescaleThreshold || (CAP && wm > kPolyLimit * kPolyLimit));
-        }
-        if (redo) {
+        {
           float mx, mn;
           if (masked)
             extremes64<true>(va, vb, lo_c, hi_c, mx, mn);
