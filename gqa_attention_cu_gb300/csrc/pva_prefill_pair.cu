@@ -73,7 +73,8 @@ struct ItemSlot {
   int t, unit, n_tiles, q0;
   int last;  // 1: no more items for this CTA
   int jb;  // first key tile (a local window skips the ones before)
-  int pad[2];
+  int empty;  // bit t: query tile t owns no row of the item
+  int pad;
 };
 
 struct PairBars {
@@ -195,6 +196,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         v.n_tiles = max(0, (hi + BN - 1) / BN - v.jb);
         v.q0 = min(it.q_start + it.t * h.tile_tokens, total_q - 2 * m_tok);
         v.last = 0;
+        v.empty = 0;
+        {
+          const int first = it.t * h.tile_tokens, lo0 = v.q0 - it.q_start;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int a = max(first, lo0 + t * m_tok);
+            const int b = min(min(first + h.tile_tokens, it.lq), lo0 + (t + 1) * m_tok);
+            if (a >= b) v.empty |= 1 << t;
+          }
+        }
         if (!(ok = publish(v))) break;
         if (v.n_tiles > 0) {
           const int g = v.unit;
@@ -261,12 +272,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto commit = [&](uint64_t* bar) {
       if (leader) mma_commit(bar);
     };
+    int empty = 0;  // bit t: query tile t of the current item owns no row
     auto issue_s = [&](int t, uint32_t kslot) {
       const uint64_t qa = sdesc_advance(qdesc, t * C::Q_TILE);
       const uint64_t ka = sdesc_advance(kdesc, kslot * C::KV_TILE);
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
+          if ((empty >> t) & 1) break;
           const uint32_t off = (kk & 3) * 32;
           mma_ss(tmem + C::COL_S + t * 128, sdesc_advance(qa, (kk >> 2) * C::Q_CHUNK + off),
                  sdesc_advance(ka, (kk >> 2) * C::KV_CHUNK + off), idesc_s, kk > 0 ? 1u : 0u);
@@ -279,9 +292,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t va = sdesc_advance(vdesc, vslot * C::KV_TILE);
       if (leader) {
 #pragma unroll
-        for (int kk = k0; kk < k1; ++kk)
+        for (int kk = k0; kk < k1; ++kk) {
+          if ((empty >> t) & 1) break;
           mma_ts(tmem + C::COL_O + t * D, tmem + C::COL_S + t * 128 + kk * 8,
                  sdesc_advance(va, kk * 16 * 128), idesc_o, (!first || kk > 0) ? 1u : 0u);
+        }
         if (k1 == BN / 16) mma_commit(&bars->o_ready[t]);
       }
     };
@@ -307,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int isl = taken % kItemSlots;
       if (!(ok = wait(&bars->item_full[isl], (taken / kItemSlots) & 1))) break;
       const int n = bars->items[isl].n_tiles, last = bars->items[isl].last;
+      empty = bars->items[isl].empty;
       __syncwarp();
       if (leader) mbar_arrive(&bars->item_empty[isl]);
       ++taken;
@@ -400,6 +416,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, mbar_wait<false>(&bars->s_full[tq], T_ & 1, abort, status));
         if (!ok) break;
         tc_fence_after();
+        if ((it.empty >> tq) & 1) {  // no row of this tile is owned: no P, no P.V
+          mbar_arrive(&bars->p_half[tq]);
+          mbar_arrive(&bars->p_full[tq]);
+          continue;
+        }
         const int J = it.jb + j;            // key tile index within the sequence
         const int k0 = min(it.kv_start + J * BN,
                            key_tile_limit(p, it.kv_start, it.lkv, total_kv) - BN);
