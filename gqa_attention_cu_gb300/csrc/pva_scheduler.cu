@@ -121,6 +121,17 @@ __device__ bool build_list(const AttnParams& p, const SchedConfig& c, const Leng
 
   int n = 0;
   if (B <= kSortMax) {
+    // An empty list (a batch of only prefill or only decode rows) skips the
+    // sort; its order and prefix are written as the sort would leave them.
+    long long members = 0;
+    for (int b = threadIdx.x; b < B; b += NT) members += member(b);
+    if (block_sum<NT>(members, scratch) == 0) {
+      for (int i = threadIdx.x; i < B; i += NT) order[i] = -1;
+      for (int i = threadIdx.x; i <= B; i += NT) prefix[i] = 0;
+      *n_out = 0;
+      *total_out = 0;
+      return true;
+    }
     int N = 1;
     while (N < B) N <<= 1;
     for (int i = threadIdx.x; i < N; i += NT) {
