@@ -146,10 +146,13 @@ def test_split_kv_decode_every_shape_and_group(d, dv, G):
     check(out, oracle.attention(q, k, v, cq, ck, G * Hkv, Hkv, 0.0, True, 0.0), "bf16")
 
 
-# Shapes the split-KV kernel serves only for small batches: with single-row
-# sequences x kv heads >= 2 x SMs they go through the tensor-core prefill
-# kernel instead (no key splits), so both routes are checked.
-@pytest.mark.parametrize("d,dv,G,Hkv", [(128, 128, 16, 2), (192, 128, 4, 8), (96, 96, 8, 4)])
+# Shapes the split-KV kernel serves only for small batches (G = 8 and 16,
+# d = 256 with G = 4, head sizes 96/192): with single-row sequences x kv
+# heads >= 2 x SMs they go through the tensor-core prefill kernel instead (no
+# key splits), so both routes are checked.
+@pytest.mark.parametrize("d,dv,G,Hkv", [(128, 128, 16, 2), (192, 128, 4, 8), (96, 96, 8, 4),
+                                        (128, 128, 8, 2), (64, 64, 8, 2), (256, 256, 8, 2),
+                                        (256, 256, 4, 2)])
 def test_many_single_row_sequences_take_the_prefill_route(d, dv, G, Hkv):
     B = 200
     g = torch.Generator().manual_seed(d + G)
