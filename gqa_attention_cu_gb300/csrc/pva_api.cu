@@ -483,7 +483,7 @@ int forward_impl(const Spec& s, void* stream_) {
     prof_mark(2, stream);
   }
   e = tc_paired(s.d, s.dv) ? launch_prefill_pair(p, s.dtype, tq, tk, tv, to, num_sms, stream)
-                           : launch_prefill_tc(p, s.dtype, tq, tk, tv, num_sms, stream);
+                           : launch_prefill_tc(p, s.dtype, tq, tk, tv, to, num_sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
   prof_mark(plan.decode ? 3 : 2, stream);
   return PVA_OK;

@@ -197,8 +197,8 @@ cudaError_t launch_padded_front(const int64_t* nonpad, int B, int q_seq, int kv_
                                 int32_t* cu_q, int32_t* cu_kv, int32_t* kv_len, cudaStream_t s);
 cudaError_t launch_prefill_f32(const AttnParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_prefill_tc(const AttnParams& p, int dtype, const CUtensorMap& tq,
-                              const CUtensorMap& tk, const CUtensorMap& tv, int num_sms,
-                              cudaStream_t s);
+                              const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& to, int num_sms, cudaStream_t s);
 // `to`: the output as [tokens, H, dv] with a {64, G, 128/G} box (epilogue
 // stores of whole query tiles).
 cudaError_t launch_prefill_pair(const AttnParams& p, int dtype, const CUtensorMap& tq,

@@ -185,7 +185,7 @@ extern "C" int pva_forward_noalloc(const void* q, const void* k, const void* v,
   }
   e = tc_paired(head_size, v_head_size)
           ? launch_prefill_pair(p, dtype, tq, tk, tv, to, ds.num_sms, stream)
-          : launch_prefill_tc(p, dtype, tq, tk, tv, ds.num_sms, stream);
+          : launch_prefill_tc(p, dtype, tq, tk, tv, to, ds.num_sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
   return PVA_OK;
 }

@@ -77,11 +77,16 @@ struct TcCfg {
   // 256, 9 at d = 192, 14 at d = 96.  The loads in flight per SM are bounded
   // by the ring: a deeper ring starts each load earlier before its tile is
   // needed, which is what hides the L2 / DRAM latency.
-  static constexpr int SLOTS_FIT = (232448 - 64 - 2048) / KV_TILE;
+  // Output staging for the epilogue's tensor stores: 4 KB per softmax warp
+  // (its 32 rows x 64 columns), at dv <= 192 only (d = dv = 256 keeps the
+  // ring slot: its items are long and its epilogue rare).
+  static constexpr int STAGE_BYTES = DV <= 192 ? 4 * 4096 : 0;
+  static constexpr int SLOTS_FIT = (232448 - 64 - 2048 - STAGE_BYTES) / KV_TILE;
   static constexpr int SLOTS = SLOTS_FIT < 16 ? SLOTS_FIT : 16;
   static_assert(SLOTS >= Q_SLOTS + 2, "K/V ring depth");
   static constexpr int OFF_RING = 0;
-  static constexpr int OFF_BAR = OFF_RING + SLOTS * KV_TILE;
+  static constexpr int OFF_STAGE = OFF_RING + SLOTS * KV_TILE;
+  static constexpr int OFF_BAR = OFF_STAGE + STAGE_BYTES;
   static constexpr int SMEM = OFF_BAR + 1024 + 1024;  // barriers/items + alignment slack
   static constexpr int TMEM_COLS = 512;
   static constexpr int COL_S = 0;                 // + BN * buffer
@@ -181,7 +186,8 @@ template <typename T, int DQK, int DV, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     pva_prefill_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap tmap_q,
                           const __grid_constant__ CUtensorMap tmap_k,
-                          const __grid_constant__ CUtensorMap tmap_v) {
+                          const __grid_constant__ CUtensorMap tmap_v,
+                          const __grid_constant__ CUtensorMap tmap_o) {
   using C = TcCfg<DQK, DV>;
   constexpr int BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
@@ -608,18 +614,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
-      // epilogue: O / l -> out (rows of this item only)
+      // epilogue: O / l -> out (rows of this item only).  When G divides 32
+      // and every row of the warp belongs to this item, the warp's 32 rows
+      // (32 / G whole tokens) leave through its 4 KB of staging and one
+      // tensor store per 64 columns; otherwise each thread stores its row.
       ok = __all_sync(0xffffffffu, mbar_wait<false>(&bars->o_done, done & 1, abort, status));
       ++done;
       if (!ok) break;
       tc_fence_after();
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+      const int own_lo = it.q_start + first, own_hi = it.q_start + min(first + m_tok, it.lq);
+      const int tok_w = it.q0 + quarter * (32 / G);
+      const bool staged =
+          C::STAGE_BYTES > 0 && 32 % G == 0 && tok_w >= own_lo && tok_w + 32 / G <= own_hi;
+      uint8_t* region = smem + C::OFF_STAGE + quarter * 4096;
 #pragma unroll 1
       for (int c = 0; c < DV; c += 32) {
         uint32_t v[32];
         tmem_ld32(t_lane + C::COL_O + c, v);
         tmem_wait_ld();
-        if (own) {
+        if (staged) {
+          const bool lo_half = (c & 63) == 0;
+          const int unit0 = lo_half ? 0 : 4;  // 16-byte units of the 128-byte row
+          if (lo_half) {  // the region is free once the previous store has read it
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int e = 8 * u;
+            uint4 w;
+            w.x = pack2<T>(__uint_as_float(v[e + 0]) * inv, __uint_as_float(v[e + 1]) * inv);
+            w.y = pack2<T>(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+            w.z = pack2<T>(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
+            w.w = pack2<T>(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
+            *reinterpret_cast<uint4*>(region + lane * 128 + (((unit0 + u) ^ (lane & 7)) << 4)) = w;
+          }
+          if (!lo_half || c + 32 >= DV) {  // the 64-column box is complete (or the last)
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tmap_o, region, c & ~63, it.unit * G, tok_w);
+              bulk_commit();
+            }
+          }
+        } else if (own) {
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 w;
@@ -635,6 +674,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars->o_free);
       gt += n;
     }
+    // Output stores must be complete before the CTA's shared memory goes.
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -645,38 +686,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <typename T, int DQK, int DV, bool CAP>
 cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                      const CUtensorMap& tv, int num_sms, cudaStream_t s) {
+                      const CUtensorMap& tv, const CUtensorMap& to, int num_sms, cudaStream_t s) {
   constexpr int smem = TcCfg<DQK, DV>::SMEM;
   auto kern = pva_prefill_tc_kernel<T, DQK, DV, CAP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_dependent(kern, dim3(num_sms), dim3(kThreads), smem, s, p, tq, tk, tv);
+  return launch_dependent(kern, dim3(num_sms), dim3(kThreads), smem, s, p, tq, tk, tv, to);
 }
 
 template <typename T, int DQK, int DV>
 cudaError_t launch_tc_cap(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, int num_sms, cudaStream_t s) {
-  return p.softcap != 0.0f ? launch_tc<T, DQK, DV, true>(p, tq, tk, tv, num_sms, s)
-                           : launch_tc<T, DQK, DV, false>(p, tq, tk, tv, num_sms, s);
+                          const CUtensorMap& tv, const CUtensorMap& to, int num_sms,
+                          cudaStream_t s) {
+  return p.softcap != 0.0f ? launch_tc<T, DQK, DV, true>(p, tq, tk, tv, to, num_sms, s)
+                           : launch_tc<T, DQK, DV, false>(p, tq, tk, tv, to, num_sms, s);
 }
 
 template <typename T>
 cudaError_t launch_tc_shape(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, int num_sms, cudaStream_t s) {
-  if (p.d == 256 && p.dv == 256) return launch_tc_cap<T, 256, 256>(p, tq, tk, tv, num_sms, s);
-  if (p.d == 192 && p.dv == 192) return launch_tc_cap<T, 192, 192>(p, tq, tk, tv, num_sms, s);
-  if (p.d == 192 && p.dv == 128) return launch_tc_cap<T, 192, 128>(p, tq, tk, tv, num_sms, s);
-  if (p.d == 96 && p.dv == 96) return launch_tc_cap<T, 96, 96>(p, tq, tk, tv, num_sms, s);
+                            const CUtensorMap& tv, const CUtensorMap& to, int num_sms,
+                            cudaStream_t s) {
+  if (p.d == 256 && p.dv == 256) return launch_tc_cap<T, 256, 256>(p, tq, tk, tv, to, num_sms, s);
+  if (p.d == 192 && p.dv == 192) return launch_tc_cap<T, 192, 192>(p, tq, tk, tv, to, num_sms, s);
+  if (p.d == 192 && p.dv == 128) return launch_tc_cap<T, 192, 128>(p, tq, tk, tv, to, num_sms, s);
+  if (p.d == 96 && p.dv == 96) return launch_tc_cap<T, 96, 96>(p, tq, tk, tv, to, num_sms, s);
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const AttnParams& p, int dtype, const CUtensorMap& tq,
-                              const CUtensorMap& tk, const CUtensorMap& tv, int num_sms,
-                              cudaStream_t s) {
-  return dtype == PVA_BF16 ? launch_tc_shape<__nv_bfloat16>(p, tq, tk, tv, num_sms, s)
-                           : launch_tc_shape<__half>(p, tq, tk, tv, num_sms, s);
+                              const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& to, int num_sms, cudaStream_t s) {
+  return dtype == PVA_BF16 ? launch_tc_shape<__nv_bfloat16>(p, tq, tk, tv, to, num_sms, s)
+                           : launch_tc_shape<__half>(p, tq, tk, tv, to, num_sms, s);
 }
 
 }  // namespace pva
