@@ -21,8 +21,9 @@
 // P_t (16-bit, two per column) overwrites the first 64 columns of S_t once
 // they have been read, and the P.V MMA takes its A operand from TMEM; the
 // next S_t MMA is issued after that P.V MMA (tcgen05 MMAs of one thread run in
-// issue order).  Shared memory (d = 128): Q0, Q1 32 KB each + 5 K/V slots of
-// 32 KB.
+// issue order).  Shared memory: Q0, Q1 (32 KB each at d = 128), a ring of
+// K/V slots (4 of 32 KB at d = 128, 10 of 16 KB at d = 64) and two 16 KB
+// output staging buffers.
 //
 // The softmax loops are specialised so that no uniform decision is taken per
 // element: softcap on/off is a template parameter, and "tile needs a mask" and
