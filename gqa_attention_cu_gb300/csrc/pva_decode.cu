@@ -15,19 +15,21 @@
 //               publishes each decoded unit through a shared-memory ring, and
 //               streams its K and V tiles of TK keys (16 KB each, rows of d
 //               contiguous elements) into a 4-stage ring.
-//   warps 1..8  compute.  A warp serves GW = min(G, 8) heads (min(G, 4) at
-//               head sizes >= 192); with more heads than that the warps split
-//               into head groups over the same tiles (G = 16, d = 128:
-//               warps 1..4 take heads 0..7 and warps 5..8 heads 8..15).  A round covers R = 32/GW keys x GW heads = 32
-//               (key, head) pairs: lane l owns DPL consecutive dims of every
-//               key (DPL = 2, 4 or 8; lanes past the head size hold zeros), forms
-//               the 32 partial dot products, and a reduce-scatter butterfly
-//               (warp shuffles) leaves the full score of pair l in lane l.
-//               Online softmax per head, probabilities shared through shared
-//               memory, O accumulated per lane over its dims of V.  Rounds
-//               are dealt to the warps across tiles, so with fewer rounds per
-//               tile than warps (small G) each warp takes whole tiles in turn.
-//   end of unit the 8 warps' (max, sum, O) are merged in a fixed order;
+//   warps 1..NW compute (NW = 12 or 8 by head shape, see DecCfg).  A warp serves
+//               GW = min(G, 8) heads (min(G, 4) at head sizes >= 192); with
+//               more heads than that the warps split into head groups over
+//               the same tiles (G = 16, d = 128: warps 1..4 take heads 0..7
+//               and warps 5..8 heads 8..15).  A round covers R = 32/GW keys
+//               x GW heads = 32 (key, head) pairs: lane l owns DPL
+//               consecutive dims of every key (DPL = 2, 4 or 8; lanes past
+//               the head size hold zeros), forms the 32 partial dot
+//               products, and a reduce-scatter butterfly (warp shuffles)
+//               leaves the full score of pair l in lane l.  Online softmax
+//               per head, probabilities shared through shared memory, O
+//               accumulated per lane over its dims of V.  Rounds are dealt to
+//               the warps across tiles, so with fewer rounds per tile than
+//               warps (small G) each warp takes whole tiles in turn.
+//   end of unit the NW warps' (max, sum, O) are merged in a fixed order;
 //               an unsplit unit writes the output row; a split unit writes
 //               its fp32 partial and the last split to finish (device-wide
 //               counter) combines all splits in split order (log-sum-exp
@@ -39,8 +41,6 @@
 namespace pva {
 namespace {
 
-constexpr int kComputeWarps = 8;
-constexpr int kThreads = 32 * (1 + kComputeWarps);
 constexpr int kStages = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kUnitSlots = 4;
@@ -55,10 +55,22 @@ struct DecCfg {
   // q and O of 8 heads (8 dims each) spilled to local memory (d = 256,
   // G = 8: 2.0 ms -> 1.16 ms for 4.6 GB of K/V).
   static constexpr int GW = DK >= 192 ? (G < 4 ? G : 4) : (G < 8 ? G : 8);
-  static constexpr int HG = G / GW;                // head groups
-  static constexpr int NWG = kComputeWarps / HG;   // warps per head group
-  static constexpr int TK = decode_tile_keys(DK, DV);  // keys per tile
   static constexpr int DPLK = dims_per_lane(DK), DPLV = dims_per_lane(DV);
+  // Compute warps: 12 where a warp serves 4 or more heads (many short
+  // rounds per tile) and a lane's q, O and 32 partial scores still fit the
+  // 128 registers that 13 warps per SM leave each thread; else 8.  A round
+  // is a long dependent chain (dot products, shuffle butterfly, softmax,
+  // P.V), and with 3 compute warps per sub-partition instead of 2 more of
+  // them overlap: d = 128, G = 4: 0.80 -> 0.76 ms (256 sequences); d = 64,
+  // G = 4 / 8 / 16: 9-12% faster.  With 1 or 2 heads per warp a tile holds
+  // few rounds and 12 warps gained nothing (d = 256, G = 1: 2% slower); the
+  // wider head shapes spill at 12.
+  static constexpr int NW =
+      GW >= 4 && GW * (DPLK > DPLV ? DPLK : DPLV) <= (DK >= 192 ? 8 : 16) ? 12 : 8;
+  static constexpr int THREADS = 32 * (1 + NW);
+  static constexpr int HG = G / GW;                // head groups
+  static constexpr int NWG = NW / HG;              // warps per head group
+  static constexpr int TK = decode_tile_keys(DK, DV);  // keys per tile
   static constexpr int LK = DK / DPLK, LV = DV / DPLV;  // lanes holding dims
   static constexpr int R = 32 / GW;                // keys per round
   static constexpr int RPT = TK / R;               // rounds per tile
@@ -66,14 +78,14 @@ struct DecCfg {
   static constexpr int V_BYTES = TK * DV * 2;
   static constexpr int STAGE = K_BYTES + V_BYTES;
   static constexpr int OFF_KV = 0;
-  static constexpr int OFF_O = kStages * STAGE;                       // [8][GW][DV] fp32
-  static constexpr int OFF_ML = OFF_O + kComputeWarps * GW * DV * 4;  // [8][GW] m, [8][GW] l
-  static constexpr int OFF_P = OFF_ML + 2 * kComputeWarps * GW * 4;   // [8][32] p
-  static constexpr int OFF_A = OFF_P + kComputeWarps * 32 * 4;        // [8][GW] alpha
-  static constexpr int OFF_BAR = OFF_A + kComputeWarps * GW * 4;
+  static constexpr int OFF_O = kStages * STAGE;             // [NW][GW][DV] fp32
+  static constexpr int OFF_ML = OFF_O + NW * GW * DV * 4;   // [NW][GW] m, [NW][GW] l
+  static constexpr int OFF_P = OFF_ML + 2 * NW * GW * 4;    // [NW][32] p
+  static constexpr int OFF_A = OFF_P + NW * 32 * 4;         // [NW][GW] alpha
+  static constexpr int OFF_BAR = OFF_A + NW * GW * 4;
   static constexpr int OFF_UNITS = OFF_BAR + 2 * kStages * 8 + 2 * kUnitSlots * 8;
   static constexpr int SMEM = OFF_UNITS + kUnitSlots * 64 + 128;
-  static_assert(G % GW == 0 && kComputeWarps % HG == 0, "head groups");
+  static_assert(G % GW == 0 && NW % HG == 0, "head groups");
   static_assert(DK % DPLK == 0 && DV % DPLV == 0, "dims per lane");
   static_assert(RPT >= 1 && TK % R == 0, "tile shorter than a round");
   static_assert(K_BYTES % 128 == 0 && V_BYTES % 128 == 0, "tile alignment");
@@ -130,8 +142,9 @@ __device__ __forceinline__ int tile_row(const AttnParams& p, const Unit& un, int
   return min(un.kv_start + un.ks + j * TK, lim - TK);
 }
 
+template <int NW>
 __device__ __forceinline__ void compute_bar_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kComputeWarps * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
 }
 
 template <typename T, int N>
@@ -173,7 +186,7 @@ __device__ __forceinline__ void load_probs(const float* src, float (&p)[G]) {
 }
 
 template <typename T, int DK, int DV, int G>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(DecCfg<DK, DV, G>::THREADS, 1)
     pva_decode_kernel(AttnParams p, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v) {
   using C = DecCfg<DK, DV, G>;
@@ -183,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~uintptr_t(127));
   float* sO = reinterpret_cast<float*>(smem + C::OFF_O);
   float* sM = reinterpret_cast<float*>(smem + C::OFF_ML);
-  float* sL = sM + kComputeWarps * GW;
+  float* sL = sM + C::NW * GW;
   float* sP = reinterpret_cast<float*>(smem + C::OFF_P);
   float* sA = reinterpret_cast<float*>(smem + C::OFF_A);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -202,11 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kComputeWarps);
+      mbar_init(&empty[s], C::NW);
     }
     for (int s = 0; s < kUnitSlots; ++s) {
       mbar_init(&unit_full[s], 1);
-      mbar_init(&unit_empty[s], kComputeWarps);
+      mbar_init(&unit_empty[s], C::NW);
     }
     fence_mbar_init();
   }
@@ -278,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ compute
-    const int cw = warp - 1;  // compute warp 0..7
+    const int cw = warp - 1;  // compute warp 0 .. NW-1
     const int hgrp = cw / C::NWG, cwg = cw % C::NWG;  // head group, warp within it
     const int hbase = hgrp * GW;                       // first head of the group
     const float NEG_INF = __int_as_float(0xff800000);
@@ -443,13 +456,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Every compute warp reaches this barrier, whether it finished its tiles
       // or gave up on a wait; the give-up decision is then read by all of
       // them at once, so no warp is ever left alone at a named barrier.
-      compute_bar_sync();
+      compute_bar_sync<C::NW>();
       if (*abort) break;
 
-      const int t = threadIdx.x - 32;  // 0..255
+      const int t = threadIdx.x - 32;  // 0 .. 32 NW - 1
       const bool split = un.S > 1;
       float* part = p.partials + (size_t)u * (G * DV + 2 * G);
-      for (int e = t; e < G * DV; e += kComputeWarps * 32) {
+      for (int e = t; e < G * DV; e += C::NW * 32) {
         const int hh = e / DV;  // head within the kv group
         const int grp = hh / GW, lh = hh - grp * GW, de = e - hh * DV;
         const int w0 = grp * C::NWG;  // the warps that served this head
@@ -478,18 +491,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (split) {
         __threadfence();
-        compute_bar_sync();
+        compute_bar_sync<C::NW>();
         if (t == 0) {
           const WsLayout L{p.B, p.Hkv};
           int* done = p.ws + L.dec_done() + (size_t)un.b * p.Hkv + un.g;
           s_last = atomicAdd(done, 1) == un.S - 1;
         }
-        compute_bar_sync();
+        compute_bar_sync<C::NW>();
         if (s_last) {
           __threadfence();
           const float* first = p.partials + (size_t)(u - un.s) * (G * DV + 2 * G);
           const size_t stride = G * DV + 2 * G;
-          for (int e = t; e < G * DV; e += kComputeWarps * 32) {
+          for (int e = t; e < G * DV; e += C::NW * 32) {
             const int hh = e / DV;
             float M = NEG_INF;
             for (int s = 0; s < un.S; ++s) M = fmaxf(M, __ldcg(first + s * stride + G * DV + hh));
@@ -507,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      compute_bar_sync();  // shared merge buffers are reused by the next unit
+      compute_bar_sync<C::NW>();  // shared merge buffers are reused by the next unit
     }
   }
   __syncthreads();
@@ -520,7 +533,8 @@ cudaError_t launch_dec(const AttnParams& p, const CUtensorMap& tk, const CUtenso
   auto kern = pva_decode_kernel<T, DK, DV, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_dependent(kern, dim3(num_sms), dim3(kThreads), smem, s, p, tk, tv);
+  return launch_dependent(kern, dim3(num_sms), dim3(DecCfg<DK, DV, G>::THREADS), smem, s, p, tk,
+                          tv);
 }
 
 template <typename T, int DK, int DV>
