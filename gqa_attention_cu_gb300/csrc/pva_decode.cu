@@ -14,7 +14,7 @@
 //   warp 0      TMA producer: draws units from a device-wide counter,
 //               publishes each decoded unit through a shared-memory ring, and
 //               streams its K and V tiles of TK keys (16 KB each, rows of d
-//               contiguous elements) into a 4-stage ring.
+//               contiguous elements) into a ring of up to 6 stages.
 //   warps 1..NW compute (NW = 12 or 8 by head shape, see DecCfg).  A warp serves
 //               GW = min(G, 8) heads (min(G, 4) at head sizes >= 192); with
 //               more heads than that the warps split into head groups over
@@ -41,7 +41,6 @@
 namespace pva {
 namespace {
 
-constexpr int kStages = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kUnitSlots = 4;
 
@@ -78,12 +77,19 @@ struct DecCfg {
   static constexpr int V_BYTES = TK * DV * 2;
   static constexpr int STAGE = K_BYTES + V_BYTES;
   static constexpr int OFF_KV = 0;
-  static constexpr int OFF_O = kStages * STAGE;             // [NW][GW][DV] fp32
+  // K/V ring: as many 32 KB stages as shared memory holds next to the merge
+  // buffers, at most 6 (6 at every shape built; 4 measured 1-5% slower:
+  // bf16_decode 0.762 -> 0.756 ms, d = 128, G = 1 2.51 -> 2.44 ms).
+  static constexpr int REST = NW * GW * DV * 4 + 2 * NW * GW * 4 + NW * 32 * 4 + NW * GW * 4 +
+                              2 * 6 * 8 + 2 * kUnitSlots * 8 + kUnitSlots * 64 + 128;
+  static constexpr int STAGES = (232448 - REST) / STAGE < 6 ? (232448 - REST) / STAGE : 6;
+  static_assert(STAGES >= 4, "K/V ring depth");
+  static constexpr int OFF_O = STAGES * STAGE;             // [NW][GW][DV] fp32
   static constexpr int OFF_ML = OFF_O + NW * GW * DV * 4;   // [NW][GW] m, [NW][GW] l
   static constexpr int OFF_P = OFF_ML + 2 * NW * GW * 4;    // [NW][32] p
   static constexpr int OFF_A = OFF_P + NW * 32 * 4;         // [NW][GW] alpha
   static constexpr int OFF_BAR = OFF_A + NW * GW * 4;
-  static constexpr int OFF_UNITS = OFF_BAR + 2 * kStages * 8 + 2 * kUnitSlots * 8;
+  static constexpr int OFF_UNITS = OFF_BAR + 2 * STAGES * 8 + 2 * kUnitSlots * 8;
   static constexpr int SMEM = OFF_UNITS + kUnitSlots * 64 + 128;
   static_assert(G % GW == 0 && NW % HG == 0, "head groups");
   static_assert(DK % DPLK == 0 && DV % DPLV == 0, "dims per lane");
@@ -200,8 +206,8 @@ __global__ void __launch_bounds__(DecCfg<DK, DV, G>::THREADS, 1)
   float* sP = reinterpret_cast<float*>(smem + C::OFF_P);
   float* sA = reinterpret_cast<float*>(smem + C::OFF_A);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* empty = full + kStages;
-  uint64_t* unit_full = empty + kStages;
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* unit_full = empty + C::STAGES;
   uint64_t* unit_empty = unit_full + kUnitSlots;
   Unit* units = reinterpret_cast<Unit*>(smem + C::OFF_UNITS);
   __shared__ int s_abort, s_last;
@@ -213,7 +219,7 @@ __global__ void __launch_bounds__(DecCfg<DK, DV, G>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     s_abort = 0;
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], C::NW);
     }
@@ -262,8 +268,8 @@ __global__ void __launch_bounds__(DecCfg<DK, DV, G>::THREADS, 1)
         if (!(ok = publish(un))) break;
         const int nt = (un.ke - un.ks + TK - 1) / TK;
         for (int j = 0; j < nt; ++j, ++cnt) {
-          const int st = cnt % kStages;
-          if (!(ok = mbar_wait(&empty[st], ((cnt / kStages) & 1) ^ 1, abort, status))) break;
+          const int st = cnt % C::STAGES;
+          if (!(ok = mbar_wait(&empty[st], ((cnt / C::STAGES) & 1) ^ 1, abort, status))) break;
           const int k0 = tile_row<TK>(p, un, j, total_kv);
           uint8_t* dk = smem + C::OFF_KV + st * C::STAGE;
           mbar_arrive_expect_tx(&full[st], C::STAGE);
@@ -284,8 +290,8 @@ __global__ void __launch_bounds__(DecCfg<DK, DV, G>::THREADS, 1)
         v.last = 1;
         publish(v);
       }
-      for (int s = 0; s < kStages; ++s) {
-        const uint32_t fills = cnt > (uint32_t)s ? (cnt - 1 - s) / kStages + 1 : 0;
+      for (int s = 0; s < C::STAGES; ++s) {
+        const uint32_t fills = cnt > (uint32_t)s ? (cnt - 1 - s) / C::STAGES + 1 : 0;
         if (fills) mbar_wait(&full[s], (fills - 1) & 1, abort, status);
       }
     }
@@ -342,8 +348,8 @@ __global__ void __launch_bounds__(DecCfg<DK, DV, G>::THREADS, 1)
       float m_run = NEG_INF, l_part = 0.0f;
 
       for (int j = 0; j < nt; ++j, ++cnt) {
-        const int st = cnt % kStages;
-        ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (cnt / kStages) & 1, abort, status));
+        const int st = cnt % C::STAGES;
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (cnt / C::STAGES) & 1, abort, status));
         if (!ok) break;
         const uint8_t* sK = smem + C::OFF_KV + st * C::STAGE;
         const uint8_t* sV = sK + C::K_BYTES;
