@@ -16,15 +16,15 @@
 //               streams its K and V tiles of TK keys (16 KB each, rows of d
 //               contiguous elements) into a ring of up to 6 stages.
 //   warps 1..NW compute (NW = 12 or 8 by head shape, see DecCfg).  A warp serves
-//               GW = min(G, 8) heads (min(G, 4) at head sizes >= 192); with
-//               more heads than that the warps split into head groups over
-//               the same tiles (G = 16, d = 128: warps 1..4 take heads 0..7
-//               and warps 5..8 heads 8..15).  A round covers R = 32/GW keys
-//               x GW heads = 32 (key, head) pairs: lane l owns DPL
-//               consecutive dims of every key (DPL = 2, 4 or 8; lanes past
-//               the head size hold zeros), forms the 32 partial dot
-//               products, and a reduce-scatter butterfly (warp shuffles)
-//               leaves the full score of pair l in lane l.  Online softmax
+//               GW = min(G, 8) heads at d = 64, min(G, 4) at larger head
+//               sizes; with more heads than that the warps split into head
+//               groups over the same tiles (G = 16, d = 128: warps 1..3 take
+//               heads 0..3, warps 4..6 heads 4..7, and so on).  A round
+//               covers R = 32/GW keys x GW heads = 32 (key, head) pairs:
+//               lane l owns DPL consecutive dims of every key (DPL = 2, 4 or
+//               8; lanes past the head size hold zeros), forms the 32
+//               partial dot products, and a reduce-scatter butterfly (warp
+//               shuffles) leaves the full score of pair l in lane l.  Online softmax
 //               per head, probabilities shared through shared memory, O
 //               accumulated per lane over its dims of V.  Rounds are dealt to
 //               the warps across tiles, so with fewer rounds per tile than
@@ -50,10 +50,15 @@ __host__ __device__ constexpr int dims_per_lane(int D) { return D <= 64 ? 2 : D 
 
 template <int DK, int DV, int G>
 struct DecCfg {
-  // Heads per warp: up to 8, or 4 at head sizes >= 192, where the per-lane
-  // q and O of 8 heads (8 dims each) spilled to local memory (d = 256,
-  // G = 8: 2.0 ms -> 1.16 ms for 4.6 GB of K/V).
-  static constexpr int GW = DK >= 192 ? (G < 4 ? G : 4) : (G < 8 ? G : 8);
+  // Heads per warp: up to 8 at d = 64, else up to 4.  At head sizes >= 192
+  // the per-lane q and O of 8 heads (8 dims each) spilled to local memory
+  // (d = 256, G = 8: 2.0 ms -> 1.16 ms for 4.6 GB of K/V); at d = 96 and 128
+  // 4 heads per warp keep a lane's arrays within the 128 registers of 12
+  // compute warps, and G = 8 / 16 ran 6% / 4% faster that way (more, shorter
+  // rounds, each K/V tile read from shared memory by 2 or 4 head groups)
+  // than with 8 heads on 8 warps; at d = 64 8 heads per warp stayed 2%
+  // faster.
+  static constexpr int GW = DK > 64 ? (G < 4 ? G : 4) : (G < 8 ? G : 8);
   static constexpr int DPLK = dims_per_lane(DK), DPLV = dims_per_lane(DV);
   // Compute warps: 12 where a warp serves 4 or more heads (many short
   // rounds per tile) and a lane's q, O and 32 partial scores still fit the
