@@ -131,8 +131,10 @@ def test_single_tile_kernel_edges(d, dv, G, causal):
 
 
 # Split-KV decode for every head-size pair of the tensor-core path and every
-# grouping it serves (G = 16 runs as two head groups of 8), with keys enough
-# for several splits and the log-sum-exp combine.
+# grouping it serves (G = 16 runs as head groups over the same tiles: two of
+# 8 heads at d = 64, four of 4 heads at larger head sizes; 12 or 8 compute
+# warps by shape), with keys enough for several splits and the log-sum-exp
+# combine.
 @pytest.mark.parametrize("d,dv", [(64, 64), (96, 96), (128, 128), (192, 192), (256, 256),
                                   (192, 128)])
 @pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
