@@ -449,7 +449,7 @@ def sched_mirror(lq, lkv, H, Hkv, d, dtype, num_sms, dv=None):
     chunk = INT_MAX
     if dec:
         keyrows = sum(b for a, b in zip(lq, lkv) if a == 1) * Hkv
-        target = num_sms * 8
+        target = num_sms * 2
         chunk = -(-keyrows // target)
         chunk = -(-chunk // 64) * 64
         chunk = max(chunk, 256)

@@ -119,16 +119,21 @@ def test_noalloc_matches_the_oracle_on_two_calls_in_a_row(lib):
 
 
 def test_noalloc_decode_with_fewer_partial_slots_than_splits(lib):
-    """d = dv = 256, G = 8, 64 long single-row sequences: the pva_forward
-    workspace would give 64 * 1 * 16 split units, the static array holds
-    fewer, so the scheduler has to choose longer splits to fit."""
-    G, Hkv, d = 8, 1, 256
+    """d = dv = 256, G = 16, 64 long single-row sequences: the split size the
+    scheduler aims at (about 2 units per SM) gives more split units than the
+    static array has partial slots for, so it has to choose longer splits to
+    fit."""
+    G, Hkv, d = 16, 1, 256
     per_unit = (G * d + 2 * G) * 4
     fit = PARTIAL_BYTES // per_unit
     B = 64
-    assert fit < B * Hkv * 16, "the case must exceed the static partial slots"
     gen = np.random.default_rng(3)
     lkv = [int(x) for x in gen.integers(5000, 8193, size=B)]
+    # the scheduler's first split size (its rule restated): keys over 2 units per SM
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    chunk = max(256, -(-(-(-sum(lkv) * Hkv // (2 * sms))) // 64) * 64)
+    units = sum(min(16, -(-n // chunk)) for n in lkv) * Hkv
+    assert units > fit, "the case must exceed the static partial slots"
     batches = [_batch([1] * B, lkv, G * Hkv, Hkv, d, d, "bf16", seed=s) for s in (11, 12)]
     _run_twice_against_oracle(lib, batches)
     # the same batch through pva_forward (room for every split) agrees too
