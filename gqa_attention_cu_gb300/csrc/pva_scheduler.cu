@@ -18,7 +18,8 @@
 //
 // One warp for B <= 32 (everything in registers), else one CTA of 128, 512 or
 // 1024 threads (by B).  Up to 16384 sequences are sorted in (dynamic) shared
-// memory (bitonic); larger batches keep their input order.
+// memory (a rank sort up to 512, bitonic above); larger batches keep their
+// input order.
 #include <limits.h>
 
 #include "pva_device.cuh"
@@ -125,49 +126,73 @@ __device__ bool build_list(const AttnParams& p, const SchedConfig& c, const Leng
     // sort; its order and prefix are written as the sort would leave them.
     long long members = 0;
     for (int b = threadIdx.x; b < B; b += NT) members += member(b);
-    if (block_sum<NT>(members, scratch) == 0) {
+    members = block_sum<NT>(members, scratch);
+    if (members == 0) {
       for (int i = threadIdx.x; i < B; i += NT) order[i] = -1;
       for (int i = threadIdx.x; i <= B; i += NT) prefix[i] = 0;
       *n_out = 0;
       *total_out = 0;
       return true;
     }
-    int N = 1;
-    while (N < B) N <<= 1;
-    for (int i = threadIdx.x; i < N; i += NT) {
-      unsigned long long key = ~0ull;
-      if (i < B && member(i)) {
-        SeqLens s = seq_lens(i);
-        key = ((unsigned long long)(unsigned)(INT_MAX - s.lkv) << 32) | (unsigned)i;
+    auto sort_key = [&](int i) -> unsigned long long {
+      if (!member(i)) return ~0ull;
+      SeqLens s = seq_lens(i);
+      return ((unsigned long long)(unsigned)(INT_MAX - s.lkv) << 32) | (unsigned)i;
+    };
+    if (B <= 512 && B <= NT) {
+      // Rank sort, one thread per sequence: a member's place is the number
+      // of members with a smaller key (keys are unique: the sequence index
+      // breaks ties; non-members hold the largest key), found in one pass
+      // over the keys in shared memory between two barriers instead of the
+      // bitonic network's log2(N) (log2(N) + 1) / 2 barriered steps (B = 256
+      // took about 22000 cycles for this list that way).
+      for (int i = threadIdx.x; i < B; i += NT) keys[i] = sort_key(i);
+      __syncthreads();
+      const int i = threadIdx.x;
+      if (i < B) {
+        const unsigned long long me = keys[i];
+        if (me != ~0ull) {
+          int rank = 0;
+#pragma unroll 4
+          for (int j = 0; j < B; ++j) rank += keys[j] < me ? 1 : 0;
+          order[rank] = i;
+          s_order[rank] = i;
+        }
       }
-      keys[i] = key;
-    }
-    __syncthreads();
-    for (int k = 2; k <= N; k <<= 1) {
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int i = threadIdx.x; i < N; i += NT) {
-          const int ixj = i ^ j;
-          if (ixj > i) {
-            const unsigned long long a = keys[i], bb = keys[ixj];
-            const bool up = (i & k) == 0;
-            if ((a > bb) == up) {
-              keys[i] = bb;
-              keys[ixj] = a;
+      n = (int)members;
+      for (int j = n + threadIdx.x; j < B; j += NT) {
+        order[j] = -1;
+        s_order[j] = -1;
+      }
+    } else {
+      int N = 1;
+      while (N < B) N <<= 1;
+      for (int i = threadIdx.x; i < N; i += NT) keys[i] = i < B ? sort_key(i) : ~0ull;
+      __syncthreads();
+      for (int k = 2; k <= N; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+          for (int i = threadIdx.x; i < N; i += NT) {
+            const int ixj = i ^ j;
+            if (ixj > i) {
+              const unsigned long long a = keys[i], bb = keys[ixj];
+              const bool up = (i & k) == 0;
+              if ((a > bb) == up) {
+                keys[i] = bb;
+                keys[ixj] = a;
+              }
             }
           }
+          __syncthreads();
         }
-        __syncthreads();
       }
+      for (int i = threadIdx.x; i < B; i += NT) {
+        const bool valid = keys[i] != ~0ull;
+        const int32_t o = valid ? (int32_t)(keys[i] & 0xffffffffu) : -1;
+        order[i] = o;
+        s_order[i] = o;
+      }
+      n = (int)members;
     }
-    long long cnt = 0;
-    for (int i = threadIdx.x; i < B; i += NT) {
-      const bool valid = keys[i] != ~0ull;
-      const int32_t o = valid ? (int32_t)(keys[i] & 0xffffffffu) : -1;
-      order[i] = o;
-      s_order[i] = o;
-      cnt += valid;
-    }
-    n = (int)block_sum<NT>(cnt, scratch);
   } else {
     // Input order: compact the members with a scan over contiguous chunks.
     const int per = (B + NT - 1) / NT;
@@ -308,23 +333,20 @@ __global__ void __launch_bounds__(NT) pva_schedule_kernel(AttnParams p, SchedCon
       // grow the chunk until the split units fit the partial slots
       for (int it = 0; it < 40; ++it) {
         long long units = 0;
-        int any_split = 0;
         for (int b = threadIdx.x; b < B; b += NT) {
           SeqLens s = seq_lens(b);
           if (s.lq == 1) {
             int sp = decode_splits(decode_keys(s.lkv, p.window),
                                    chunk > INT_MAX ? INT_MAX : (int)chunk);
             units += (long long)sp * p.Hkv;
-            any_split |= sp > 1;
           }
         }
         units = block_sum<NT>(units, scratch);
-        const long long splits = block_sum<NT>(any_split, scratch);
-        if (splits == 0 || units <= p.dec_cap_units) break;
+        // one unit per (sequence, kv head) means that nothing is split
+        if (units == cnt * p.Hkv || units <= p.dec_cap_units) break;
         chunk *= 2;
       }
       if (threadIdx.x == 0) s_chunk = chunk > INT_MAX ? INT_MAX : (int)chunk;
-      (void)cnt;
     } else if (threadIdx.x == 0) {
       s_chunk = INT_MAX;
     }
