@@ -50,6 +50,7 @@ __device__ __forceinline__ float table(const void* t, int idx, int is_f16) {
 }
 
 __global__ void __launch_bounds__(1024) pva_cache_meta_kernel(CacheStep c) {
+  allow_next_grid();  // the append kernel may start its launch now
   __shared__ uint32_t s_bad;
   if (threadIdx.x == 0) s_bad = (atomicOr(c.status, 0u) & PVA_DEV_KV_CACHE) ? 1u : 0u;
   __syncthreads();
@@ -104,6 +105,9 @@ __device__ __forceinline__ void pair_dims(int k, int rot, int interleaved, int& 
 
 template <typename T>
 __global__ void __launch_bounds__(256) pva_cache_prep_kernel(CacheStep c) {
+  // a programmatic dependent of the metadata kernel, whose starts it reads
+  allow_next_grid();
+  wait_prior_grid();
   const int hd = c.d / 2;  // pairs per head row
   const long long nq = c.rot > 0 ? (long long)c.B * c.q_seq * c.H * hd : 0;
   const long long nk = (long long)c.B * c.k_seq * c.Hkv * hd;
@@ -170,11 +174,11 @@ cudaError_t launch_cache_front(const CacheStep& c, cudaStream_t s) {
   const long long want = (n + 255) / 256, cap = (long long)(sms > 0 ? sms : 1) * 8;
   const int grid = (int)(want < cap ? want : cap);
   switch (c.dtype) {
-    case PVA_F32: pva_cache_prep_kernel<float><<<grid, 256, 0, s>>>(c); break;
-    case PVA_F16: pva_cache_prep_kernel<__half><<<grid, 256, 0, s>>>(c); break;
-    default: pva_cache_prep_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(c); break;
+    case PVA_F32: return launch_dependent(pva_cache_prep_kernel<float>, dim3(grid), dim3(256), 0, s, c);
+    case PVA_F16: return launch_dependent(pva_cache_prep_kernel<__half>, dim3(grid), dim3(256), 0, s, c);
+    default:
+      return launch_dependent(pva_cache_prep_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, c);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace pva

@@ -257,7 +257,10 @@ __global__ void __launch_bounds__(NT) pva_schedule_kernel(AttnParams p, SchedCon
 
   // The compute kernels are launched as programmatic dependents: let them
   // start their set-up now; they wait for this grid before reading its output.
+  // This grid is one too (its launch overlaps the end of the work before it),
+  // so it waits for that work before reading the offsets.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  wait_prior_grid();
 
   const int B = p.B;
   const WsLayout L{B, p.Hkv};
@@ -392,6 +395,7 @@ __device__ __forceinline__ long long warp_sum_ll(long long v) {
 // counters and status bits are identical.
 __global__ void __launch_bounds__(32) pva_schedule_warp_kernel(AttnParams p, SchedConfig c) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  wait_prior_grid();  // launched as a dependent of the work before it
   const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x, B = p.B;
   const WsLayout L{B, p.Hkv};
@@ -534,21 +538,22 @@ cudaError_t launch_padded_front(const int64_t* nonpad, int B, int q_seq, int kv_
 }
 
 cudaError_t launch_scheduler(const AttnParams& p, const SchedConfig& c, cudaStream_t s) {
+  // Programmatic dependents of the work before them (each waits for it first).
   if (p.B <= 32)
-    pva_schedule_warp_kernel<<<1, 32, 0, s>>>(p, c);
-  else if (p.B <= 128)
-    pva_schedule_kernel<128><<<1, 128, sched_smem_bytes(p.B), s>>>(p, c);
-  else if (p.B <= 512)
-    pva_schedule_kernel<512><<<1, 512, sched_smem_bytes(p.B), s>>>(p, c);
-  else {
-    // more than 48 KB of dynamic shared memory needs the opt-in
-    cudaError_t e = cudaFuncSetAttribute(pva_schedule_kernel<1024>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sched_smem_bytes(kSortMax));
-    if (e != cudaSuccess) return e;
-    pva_schedule_kernel<1024><<<1, 1024, sched_smem_bytes(p.B), s>>>(p, c);
-  }
-  return cudaGetLastError();
+    return launch_dependent(pva_schedule_warp_kernel, dim3(1), dim3(32), 0, s, p, c);
+  if (p.B <= 128)
+    return launch_dependent(pva_schedule_kernel<128>, dim3(1), dim3(128), sched_smem_bytes(p.B),
+                            s, p, c);
+  if (p.B <= 512)
+    return launch_dependent(pva_schedule_kernel<512>, dim3(1), dim3(512), sched_smem_bytes(p.B),
+                            s, p, c);
+  // more than 48 KB of dynamic shared memory needs the opt-in
+  cudaError_t e = cudaFuncSetAttribute(pva_schedule_kernel<1024>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sched_smem_bytes(kSortMax));
+  if (e != cudaSuccess) return e;
+  return launch_dependent(pva_schedule_kernel<1024>, dim3(1), dim3(1024),
+                          sched_smem_bytes(p.B), s, p, c);
 }
 
 }  // namespace pva
