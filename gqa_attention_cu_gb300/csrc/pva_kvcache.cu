@@ -51,6 +51,7 @@ __device__ __forceinline__ float table(const void* t, int idx, int is_f16) {
 
 __global__ void __launch_bounds__(1024) pva_cache_meta_kernel(CacheStep c) {
   allow_next_grid();  // the append kernel may start its launch now
+  wait_prior_grid();  // launched as a dependent of the work before it
   __shared__ uint32_t s_bad;
   if (threadIdx.x == 0) s_bad = (atomicOr(c.status, 0u) & PVA_DEV_KV_CACHE) ? 1u : 0u;
   __syncthreads();
@@ -161,8 +162,7 @@ __global__ void __launch_bounds__(256) pva_cache_prep_kernel(CacheStep c) {
 }  // namespace
 
 cudaError_t launch_cache_front(const CacheStep& c, cudaStream_t s) {
-  pva_cache_meta_kernel<<<1, 1024, 0, s>>>(c);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(pva_cache_meta_kernel, dim3(1), dim3(1024), 0, s, c);
   if (e != cudaSuccess) return e;
   const long long hd = c.d / 2;
   const long long n = (c.rot > 0 ? (long long)c.B * c.q_seq * c.H * hd : 0) +

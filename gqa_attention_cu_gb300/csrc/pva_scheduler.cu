@@ -518,6 +518,9 @@ __global__ void __launch_bounds__(32) pva_schedule_warp_kernel(AttnParams p, Sch
 // [0, kv_seq] is stored as -1, which the scheduler reports as PVA_DEV_KV_LEN.
 __global__ void pva_padded_front_kernel(const int64_t* nonpad, int B, int q_seq, int kv_seq,
                                         int32_t* cu_q, int32_t* cu_kv, int32_t* kv_len) {
+  // a programmatic dependent of the work before it, like every kernel here
+  allow_next_grid();
+  wait_prior_grid();
   for (int b = blockIdx.x * blockDim.x + threadIdx.x; b <= B; b += gridDim.x * blockDim.x) {
     cu_q[b] = b * q_seq;
     cu_kv[b] = b * kv_seq;
@@ -531,10 +534,8 @@ __global__ void pva_padded_front_kernel(const int64_t* nonpad, int B, int q_seq,
 cudaError_t launch_padded_front(const int64_t* nonpad, int B, int q_seq, int kv_seq,
                                 int32_t* cu_q, int32_t* cu_kv, int32_t* kv_len, cudaStream_t s) {
   const int threads = 256, blocks = (B + threads) / threads;
-  pva_padded_front_kernel<<<blocks < 1024 ? blocks : 1024, threads, 0, s>>>(nonpad, B, q_seq,
-                                                                          kv_seq, cu_q, cu_kv,
-                                                                          kv_len);
-  return cudaGetLastError();
+  return launch_dependent(pva_padded_front_kernel, dim3(blocks < 1024 ? blocks : 1024),
+                          dim3(threads), 0, s, nonpad, B, q_seq, kv_seq, cu_q, cu_kv, kv_len);
 }
 
 cudaError_t launch_scheduler(const AttnParams& p, const SchedConfig& c, cudaStream_t s) {
