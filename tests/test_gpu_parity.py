@@ -525,6 +525,26 @@ def test_scheduler_small_batches_match_host_mirror(B, cfg):
     assert words == sched_mirror(lq, lkv, H, Hkv, d, dtype, sms, dv)
 
 
+@pytest.mark.parametrize("B", [33, 128, 129, 300, 512, 513, 1000])
+def test_scheduler_ties_in_key_length_match_host_mirror(B):
+    """Many sequences share an L_kv, so the order among them rests on the
+    index tie-break alone: the rank sort (B <= 512) and the bitonic network
+    above it must both put equal lengths in index order."""
+    g = torch.Generator().manual_seed(1000 + B)
+    lq = torch.randint(0, 300, (B,), generator=g)
+    lq = torch.where(torch.rand(B, generator=g) < 0.5, torch.ones_like(lq), lq)
+    # key lengths from only five values (decode rows) or lq + one of five pasts
+    lkv = torch.where(lq == 1, 1 + 1000 * torch.randint(1, 6, (B,), generator=g),
+                      lq + 512 * torch.randint(0, 5, (B,), generator=g))
+    lq, lkv = lq.tolist(), lkv.tolist()
+    dev = torch.device("cuda:0")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for H, Hkv, d, dv in ((32, 8, 128, 128), (64, 4, 64, 64)):
+        words = pva.pva_schedule(workloads.cu_from_lengths(lq).to(dev),
+                                 workloads.cu_from_lengths(lkv).to(dev), B, H, Hkv, d, dv, 1, 2)
+        assert words == sched_mirror(lq, lkv, H, Hkv, d, 2, sms, dv)
+
+
 @pytest.mark.parametrize("B", [2048, 2049, 4096, 9000, 16384, 16385])
 def test_scheduler_large_batches_match_host_mirror(B):
     """Up to 16384 sequences are sorted longest first on the device (shared
