@@ -174,8 +174,10 @@ cudaError_t launch_cache_front(const CacheStep& c, cudaStream_t s) {
   const long long want = (n + 255) / 256, cap = (long long)(sms > 0 ? sms : 1) * 8;
   const int grid = (int)(want < cap ? want : cap);
   switch (c.dtype) {
-    case PVA_F32: return launch_dependent(pva_cache_prep_kernel<float>, dim3(grid), dim3(256), 0, s, c);
-    case PVA_F16: return launch_dependent(pva_cache_prep_kernel<__half>, dim3(grid), dim3(256), 0, s, c);
+    case PVA_F32:
+      return launch_dependent(pva_cache_prep_kernel<float>, dim3(grid), dim3(256), 0, s, c);
+    case PVA_F16:
+      return launch_dependent(pva_cache_prep_kernel<__half>, dim3(grid), dim3(256), 0, s, c);
     default:
       return launch_dependent(pva_cache_prep_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, c);
   }
